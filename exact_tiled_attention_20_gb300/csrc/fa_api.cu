@@ -1,0 +1,224 @@
+// fa_api.cu -- the C ABI: argument validation, TMA tensor-map encoding, dispatch.
+//
+// Nothing here allocates device memory.  Every call validates its arguments before it
+// enqueues anything, launches on the caller's stream and returns without synchronising.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa_internal.h"
+
+namespace fa {
+
+// Sticky device status word written by kernels whose bounded waits give up.  Host code
+// never dereferences the symbol: it resolves the device address per device.
+__device__ int g_fa_device_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+struct DeviceInfo {
+    int num_sms = 0;
+    int* status = nullptr;  // device address of g_fa_device_status
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+bool device_info(DeviceInfo* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (d.num_sms == 0) {
+        int sms = 0;
+        void* st = nullptr;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms <= 0)
+            return false;
+        if (cudaGetSymbolAddress(&st, g_fa_device_status) != cudaSuccess) return false;
+        d.status = static_cast<int*>(st);
+        d.num_sms = sms;
+    }
+    *out = d;
+    return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+bool encode_tmap_4d(CUtensorMap* map, const void* base, bool bf16, uint64_t dim0, uint64_t dim1,
+                    uint64_t dim2, uint64_t dim3, uint32_t box_rows) {
+    return encode_tmap_4d_box(map, base, bf16, dim0, dim1, dim2, dim3, 1, box_rows);
+}
+
+bool encode_tmap_4d_box(CUtensorMap* map, const void* base, bool bf16, uint64_t dim0,
+                        uint64_t dim1, uint64_t dim2, uint64_t dim3, uint32_t box1,
+                        uint32_t box2) {
+    EncodeTiledFn enc = get_encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {dim0, dim1, dim2, dim3};
+    const cuuint64_t strides[3] = {dim0 * 2, dim0 * dim1 * 2, dim0 * dim1 * dim2 * 2};
+    const cuuint32_t box[4] = {64, box1, box2, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                     4, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool ensure_smem_attr(const void* func, int bytes, int* done_flags) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    if (__atomic_load_n(&done_flags[dev], __ATOMIC_ACQUIRE)) return true;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess)
+        return false;
+    __atomic_store_n(&done_flags[dev], 1, __ATOMIC_RELEASE);
+    return true;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq,
+                 int Sk, int Hq, int Hkv, int D, float scale, int causal, fa_dtype dtype,
+                 fa_stream_t stream) {
+    if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_INVALID_ARG;
+    if (B <= 0 || Sq <= 0 || Sk <= 0 || Hq <= 0 || Hkv <= 0) return FA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_UNSUPPORTED;
+    if (D != 64 && D != 96 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+    // TMA coordinates are 32-bit signed; the batch and sequence extents must fit.
+    if ((long long)B * Sq > 0x7fffffffLL || (long long)B * Sk > 0x7fffffffLL)
+        return FA_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    if (!device_info(&di)) return FA_ERR_CUDA;
+    FwdArgs a{q, k, v, o, lse, B, Sq, Sk, Hq, Hkv, D, scale, causal, dtype == FA_BF16,
+              di.num_sms, di.status};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    switch (D) {
+        case 64: return launch_fwd_d64(a, s);
+        case 96: return launch_fwd_d96(a, s);
+        case 128: return launch_fwd_d128(a, s);
+        default: return launch_fwd_d256(a, s);
+    }
+}
+
+size_t fa_decode_workspace_bytes(int B, int Hq, int D, int num_splits) {
+    if (B <= 0 || Hq <= 0 || D <= 0 || num_splits <= 0) return 0;
+    const size_t rows = (size_t)B * Hq * num_splits;
+    const size_t o_bytes = (rows * D * sizeof(float) + 255) & ~size_t(255);
+    const size_t l_bytes = (rows * sizeof(float) + 255) & ~size_t(255);
+    return o_bytes + l_bytes;
+}
+
+int fa_decode_default_splits(int B, int Hkv, int max_kv_len, int num_sms) {
+    if (B <= 0 || Hkv <= 0 || max_kv_len <= 0) return -1;
+    if (num_sms <= 0) {
+        DeviceInfo di;
+        if (!device_info(&di)) return -1;
+        num_sms = di.num_sms;
+    }
+    // Aim for about eight work items per SM (lengths vary, so about half the chunks of
+    // the longest sequence exist for an average one), with chunks of at least 256 keys.
+    const long long groups = (long long)B * Hkv;
+    long long ns = (8LL * num_sms + groups - 1) / groups;
+    const long long max_by_len = ((long long)max_kv_len + 255) / 256;
+    if (ns > max_by_len) ns = max_by_len;
+    if (ns > 1024) ns = 1024;
+    if (ns < 1) ns = 1;
+    return (int)ns;
+}
+
+fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* kv_lens, void* o, float* lse, int B, int Hq, int Hkv,
+                            int D, int Smax, float scale, int num_splits, void* workspace,
+                            size_t workspace_bytes, fa_dtype dtype, fa_stream_t stream) {
+    if (!q || !k_cache || !v_cache || !kv_lens || !o) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+        (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
+        return FA_ERR_INVALID_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Smax <= 0) return FA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_UNSUPPORTED;
+    if (D != 128 && D != 64) return FA_ERR_UNSUPPORTED;
+    if (Hq / Hkv > 16) return FA_ERR_UNSUPPORTED;
+    if ((long long)B * Smax > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    if (!device_info(&di)) return FA_ERR_CUDA;
+    if (num_splits <= 0) num_splits = fa_decode_default_splits(B, Hkv, Smax, di.num_sms);
+    if (num_splits > Smax) num_splits = Smax;
+    const size_t need = fa_decode_workspace_bytes(B, Hq, D, num_splits);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FA_ERR_WORKSPACE;
+    const size_t rows = (size_t)B * Hq * num_splits;
+    float* o_part = static_cast<float*>(workspace);
+    float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                               ((rows * D * sizeof(float) + 255) & ~size_t(255)));
+    DecodeArgs a{q, k_cache, v_cache, kv_lens, o, lse, B, Hq, Hkv, D, Smax, scale, num_splits,
+                 o_part, lse_part, dtype == FA_BF16, di.num_sms, di.status};
+    return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char* fa_status_string(fa_status s) {
+    switch (s) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: unsupported head dim, dtype or size";
+        case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: decode workspace missing or too small";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA call failed";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel gave up on a bounded wait";
+        default: return "unknown fa_status";
+    }
+}
+
+fa_status fa_last_device_status(void) {
+    DeviceInfo di;
+    if (!device_info(&di)) return FA_ERR_CUDA;
+    int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaMemcpy(&v, di.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(di.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return FA_ERR_CUDA;
+    }
+    return v == 0 ? FA_OK : (fa_status)v;
+}
+
+}  // extern "C"

@@ -1,0 +1,494 @@
+// fa_fwd.cuh -- exact attention forward for sm_103a (tcgen05 + TMA, warp-specialised).
+//
+// What is computed: O = softmax(scale * Q K^T [+ causal mask]) V with the per-row
+// log-sum-exp, for [B, S, H, D] tensors with grouped-query heads (page
+// "flash-attention-v100", "How to use FlashAttention"; bottom-right causal mask from
+// "Changelog", "2.1: Change behavior of causal flag").
+//
+// How (FlashAttention-2 work partitioning, page "ampere_flash_attention_from_scratch";
+// the RTX 3080 kernel there is prior art, this is a Blackwell design):
+//  * A persistent CTA per SM walks work tiles (b, h, query block of NQ x 128 rows); the
+//    query blocks of one head are adjacent in the walk so concurrent CTAs share K/V in L2.
+//  * Warp roles: one TMA producer warp streams Q once per tile and K/V tiles of BN keys
+//    through an NS-stage ring (full / empty mbarriers); one MMA warp issues tcgen05.mma;
+//    NQ softmax warpgroups own one 128-row Q tile each (thread = row = TMEM lane).
+//  * S = Q K^T: A = Q and B = K from 128-byte-swizzled shared memory, fp32 accumulator in
+//    TMEM.  The softmax warpgroup reads S from TMEM, applies the mask, keeps the running
+//    max m and sum l (online softmax in base 2 with scale*log2(e) folded into one FMA),
+//    rounds P to 16 bits and writes it back into the same TMEM columns.
+//  * O += P V: A = P straight from TMEM, B = V (MN-major) from shared memory.  O stays in
+//    TMEM for the whole KV loop; it is rescaled only when a row max grows by more than
+//    2^8 (the sum l uses the same stale max, so the final O / l is exact).
+//  * With NQ = 2 the two Q tiles ping-pong: the tensor pipe runs one tile's GEMMs while
+//    the other tile's softmax runs.  With NQ = 1 S is double-buffered instead.
+//  * Epilogue: O / l rounded to 16 bits and stored row by row; LSE = (m + log2 l) ln 2.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+struct FwdParams {
+    int B, Sq, Sk, Hq, Hkv, group;
+    int causal;
+    float scale_log2;  // softmax scale * log2(e)
+    int num_qb;        // query blocks of NQ * 128 rows per (b, h)
+    int num_tiles;     // B * Hq * num_qb
+    void* o;           // [B, Sq, Hq, D]
+    float* lse;        // [B, Hq, Sq] or null
+    int* status;       // sticky device status word
+};
+
+template <int D_, int BN_, int NQ_, int NS_>
+struct FwdConfig {
+    static constexpr int D = D_;
+    static constexpr int BM = 128;
+    static constexpr int BN = BN_;
+    static constexpr int NQ = NQ_;
+    static constexpr int NS = NS_;
+    static constexpr int DA = (D + 63) / 64;  // 128-byte column atoms per row
+    static constexpr int kQBytes = BM * DA * 128;
+    static constexpr int kKVBytes = BN * DA * 128;
+    static constexpr int kSlots = (NQ == 1) ? 2 : NQ;  // S buffers in TMEM
+    static constexpr int kOCol0 = kSlots * BN;        // first O column in TMEM
+    static constexpr int kTmemCols = 512;
+    static_assert(kOCol0 + NQ * D <= kTmemCols, "TMEM budget");
+    static_assert(D % 32 == 0 && BN % 64 == 0, "tile shape");
+    static constexpr int kThreads = 128 * NQ + 64;
+    static constexpr int kProducerWarp = 4 * NQ;
+    static constexpr int kMmaWarp = 4 * NQ + 1;
+    // barrier indices
+    static constexpr int kBarQFull = 0;
+    static constexpr int kBarQEmpty = kBarQFull + NQ;
+    static constexpr int kBarKFull = kBarQEmpty + NQ;
+    static constexpr int kBarKEmpty = kBarKFull + NS;
+    static constexpr int kBarVFull = kBarKEmpty + NS;
+    static constexpr int kBarVEmpty = kBarVFull + NS;
+    static constexpr int kBarSFull = kBarVEmpty + NS;
+    static constexpr int kBarPFull = kBarSFull + kSlots;
+    static constexpr int kBarODone = kBarPFull + NQ;
+    static constexpr int kBarODrained = kBarODone + NQ;
+    static constexpr int kBarFinal = kBarODrained + NQ;
+    static constexpr int kNumBars = kBarFinal + 1;
+    static constexpr int kTileBytes = NQ * kQBytes + 2 * NS * kKVBytes;
+    static constexpr int kSmemBytes = 1024 /* alignment slack */ + kTileBytes + 8 * kNumBars + 16;
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct TileCoord {
+    int b, h, hk, m0, n_kv;
+};
+
+template <class C>
+__device__ __forceinline__ TileCoord decode_tile(const FwdParams& p, int t) {
+    TileCoord c;
+    const int qb_raw = t % p.num_qb;
+    const int bh = t / p.num_qb;
+    // causal: the longest query block of each head first
+    const int qb = p.causal ? (p.num_qb - 1 - qb_raw) : qb_raw;
+    c.h = bh % p.Hq;
+    c.b = bh / p.Hq;
+    c.hk = c.h / p.group;
+    c.m0 = qb * (C::NQ * C::BM);
+    int kv_end = p.Sk;
+    if (p.causal) {
+        const int last_row = min(p.Sq, c.m0 + C::NQ * C::BM) - 1;
+        kv_end = min(kv_end, last_row + (p.Sk - p.Sq) + 1);
+    }
+    c.n_kv = kv_end > 0 ? (kv_end + C::BN - 1) / C::BN : 0;
+    return c;
+}
+
+template <class C, bool kBF16>
+__global__ void __launch_bounds__(C::kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t base = (raw_u32 + 1023u) & ~1023u;
+    uint8_t* base_gen = smem_raw + (base - raw_u32);
+
+    const uint32_t sQ = base;
+    const uint32_t sK = sQ + C::NQ * C::kQBytes;
+    const uint32_t sV = sK + C::NS * C::kKVBytes;
+    const uint32_t sBar = sV + C::NS * C::kKVBytes;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_gen + C::kTileBytes + 8 * C::kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    auto bar = [&](int i) -> uint32_t { return sBar + 8u * (uint32_t)i; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const WaitCtx wc{abort_flag, p.status};
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kNumBars; ++i) {
+            const bool by_warpgroup = (i >= C::kBarPFull && i < C::kBarPFull + C::NQ) ||
+                                      (i >= C::kBarODrained && i < C::kBarODrained + C::NQ);
+            mbar_init(bar(i), by_warpgroup ? 128u : 1u);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == C::kMmaWarp) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == C::kProducerWarp && lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+
+    if (warp == C::kProducerWarp) {
+        // ------------------------------------------------------------ TMA producer --
+        if (lane == 0) {
+            uint32_t kv_it = 0, tcount = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+                const TileCoord c = decode_tile<C>(p, t);
+                if (c.n_kv == 0) continue;
+                for (int q = 0; q < C::NQ && ok; ++q) {
+                    ok = mbar_wait(bar(C::kBarQEmpty + q), (tcount & 1u) ^ 1u, wc);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(C::kBarQFull + q), C::kQBytes);
+                    for (int a = 0; a < C::DA; ++a)
+                        tma_load_4d(sQ + q * C::kQBytes + a * (C::BM * 128), &tm_q,
+                                    bar(C::kBarQFull + q), a * 64, c.h, c.m0 + q * C::BM, c.b);
+                }
+                for (int j = 0; j < c.n_kv && ok; ++j) {
+                    const uint32_t st = kv_it % C::NS;
+                    const uint32_t ph = ((kv_it / C::NS) & 1u) ^ 1u;
+                    ok = mbar_wait(bar(C::kBarKEmpty + st), ph, wc);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(C::kBarKFull + st), C::kKVBytes);
+                    for (int a = 0; a < C::DA; ++a)
+                        tma_load_4d(sK + st * C::kKVBytes + a * (C::BN * 128), &tm_k,
+                                    bar(C::kBarKFull + st), a * 64, c.hk, j * C::BN, c.b);
+                    ok = mbar_wait(bar(C::kBarVEmpty + st), ph, wc);
+                    if (!ok) {
+                        // K of this iteration is in flight: account for it in the drain
+                        mbar_wait_drain(bar(C::kBarKFull + st), (kv_it / C::NS) & 1u);
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(C::kBarVFull + st), C::kKVBytes);
+                    for (int a = 0; a < C::DA; ++a)
+                        tma_load_4d(sV + st * C::kKVBytes + a * (C::BN * 128), &tm_v,
+                                    bar(C::kBarVFull + st), a * 64, c.hk, j * C::BN, c.b);
+                    ++kv_it;
+                }
+                ++tcount;
+            }
+            // Drain: every copy this warp started has landed before shared memory goes.
+            // The last NS iterations hold the last use of each stage.
+            for (uint32_t d = 0; d < (uint32_t)C::NS && d < kv_it; ++d) {
+                const uint32_t last = kv_it - 1 - d;
+                const uint32_t st = last % C::NS;
+                mbar_wait_drain(bar(C::kBarKFull + st), (last / C::NS) & 1u);
+                mbar_wait_drain(bar(C::kBarVFull + st), (last / C::NS) & 1u);
+            }
+            if (tcount > 0)
+                for (int q = 0; q < C::NQ; ++q)
+                    mbar_wait_drain(bar(C::kBarQFull + q), (tcount - 1) & 1u);
+        }
+        __syncwarp();
+    } else if (warp == C::kMmaWarp) {
+        // ------------------------------------------------------------- MMA issuer ----
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = make_idesc_f16(128, C::BN, kBF16, false, false);
+            constexpr uint32_t idesc_o = make_idesc_f16(128, C::D, kBF16, false, true);
+            uint32_t kv_it = 0, tcount = 0, it = 0;
+            bool ok = true;
+
+            auto issue_s = [&](int q, uint32_t kst, uint32_t slot) {
+                const uint32_t d = tmem + slot * C::BN;
+#pragma unroll
+                for (int kk = 0; kk < C::D / 16; ++kk) {
+                    const uint32_t a_addr =
+                        sQ + q * C::kQBytes + (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
+                    const uint32_t b_addr =
+                        sK + kst * C::kKVBytes + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32;
+                    umma_ss(d, make_sdesc_sw128(a_addr, 16, 1024), make_sdesc_sw128(b_addr, 16, 1024),
+                            idesc_s, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](int q, uint32_t vst, uint32_t slot, bool acc) {
+                const uint32_t d = tmem + C::kOCol0 + q * C::D;
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk) {
+                    const uint32_t a_tmem = tmem + slot * C::BN + kk * 8;
+                    const uint32_t b_addr = sV + vst * C::kKVBytes + kk * (16 * 128);
+                    umma_ts(d, a_tmem, make_sdesc_sw128(b_addr, C::BN * 128, 1024), idesc_o,
+                            (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            auto slot_of = [&](int q, uint32_t iter) -> uint32_t {
+                return C::NQ == 1 ? (iter & 1u) : (uint32_t)q;
+            };
+
+            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+                const TileCoord c = decode_tile<C>(p, t);
+                const int n = c.n_kv;
+                if (n == 0) continue;
+                for (int q = 0; q < C::NQ && ok; ++q) ok = mbar_wait(bar(C::kBarQFull + q), tcount & 1u, wc);
+                if (!ok) break;
+                {
+                    const uint32_t st = kv_it % C::NS;
+                    ok = mbar_wait(bar(C::kBarKFull + st), (kv_it / C::NS) & 1u, wc);
+                    if (!ok) break;
+                    tc_fence_after();
+                    for (int q = 0; q < C::NQ; ++q) {
+                        issue_s(q, st, slot_of(q, it));
+                        umma_commit(bar(C::kBarSFull + slot_of(q, it)));
+                    }
+                    umma_commit(bar(C::kBarKEmpty + st));
+                    if (n == 1)
+                        for (int q = 0; q < C::NQ; ++q) umma_commit(bar(C::kBarQEmpty + q));
+                }
+                for (int j = 0; j < n && ok; ++j) {
+                    const uint32_t cur = kv_it + j;
+                    const uint32_t st = cur % C::NS;
+                    const uint32_t nst = (cur + 1) % C::NS;
+                    const bool more = (j + 1 < n);
+                    if (C::NQ == 1 && more) {
+                        ok = mbar_wait(bar(C::kBarKFull + nst), ((cur + 1) / C::NS) & 1u, wc);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(0, nst, slot_of(0, it + 1));
+                        umma_commit(bar(C::kBarSFull + slot_of(0, it + 1)));
+                        umma_commit(bar(C::kBarKEmpty + nst));
+                        if (j + 2 == n) umma_commit(bar(C::kBarQEmpty + 0));
+                    }
+                    ok = mbar_wait(bar(C::kBarVFull + st), (cur / C::NS) & 1u, wc);
+                    if (!ok) break;
+                    for (int q = 0; q < C::NQ && ok; ++q) {
+                        ok = mbar_wait(bar(C::kBarPFull + q), it & 1u, wc);
+                        if (ok && j == 0 && tcount > 0)
+                            ok = mbar_wait(bar(C::kBarODrained + q), (tcount - 1) & 1u, wc);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(q, st, slot_of(q, it), j > 0);
+                        umma_commit(bar(C::kBarODone + q));
+                        if (C::NQ > 1 && more) {
+                            if (q == 0) {
+                                ok = mbar_wait(bar(C::kBarKFull + nst), ((cur + 1) / C::NS) & 1u, wc);
+                                if (!ok) break;
+                                tc_fence_after();
+                            }
+                            issue_s(q, nst, slot_of(q, it + 1));
+                            umma_commit(bar(C::kBarSFull + slot_of(q, it + 1)));
+                            if (q == C::NQ - 1) umma_commit(bar(C::kBarKEmpty + nst));
+                            if (j + 2 == n) umma_commit(bar(C::kBarQEmpty + q));
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit(bar(C::kBarVEmpty + st));
+                    ++it;
+                }
+                kv_it += n;
+                ++tcount;
+            }
+            // Every MMA issued has completed before TMEM and shared memory are released.
+            umma_commit(bar(C::kBarFinal));
+            mbar_wait_drain(bar(C::kBarFinal), 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------ softmax warpgroups ----
+        const int q = warp >> 2;
+        const int wq = warp & 3;           // TMEM lane quadrant of this warp
+        const int r = wq * 32 + lane;      // row within the 128-row Q tile
+        const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+        const uint32_t tO = lane_base + C::kOCol0 + q * C::D;
+        const float kNegInf = -__int_as_float(0x7f800000);
+        constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
+        const int off = p.Sk - p.Sq;           // bottom-right causal alignment
+        uint32_t it = 0;
+        bool ok = true;
+
+        for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+            const TileCoord c = decode_tile<C>(p, t);
+            const int row = c.m0 + q * C::BM + r;
+            const size_t o_row = ((size_t)c.b * p.Sq + row) * p.Hq + c.h;
+            uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + o_row * C::D;
+            if (c.n_kv == 0) {
+                if (row < p.Sq) {
+#pragma unroll
+                    for (int d = 0; d < C::D; d += 8) st_global_v4(orow + d, 0u, 0u, 0u, 0u);
+                    if (p.lse) p.lse[((size_t)c.b * p.Hq + c.h) * p.Sq + row] = kNegInf;
+                }
+                continue;
+            }
+            float m_run = kNegInf;  // running max, log2 units (raw score * scale * log2 e)
+            float l_run = 0.f;
+            const int tile_row0 = c.m0 + q * C::BM;
+
+            for (int j = 0; j < c.n_kv; ++j) {
+                const uint32_t slot = (C::NQ == 1) ? (it & 1u) : (uint32_t)q;
+                const uint32_t spar = (C::NQ == 1) ? ((it >> 1) & 1u) : (it & 1u);
+                ok = mbar_wait(bar(C::kBarSFull + slot), spar, wc);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t tS = lane_base + slot * C::BN;
+                float s[C::BN];
+#pragma unroll
+                for (int ch = 0; ch < C::BN / 32; ++ch) {
+                    uint32_t u[32];
+                    tmem_ld_32x32b_x32(tS + ch * 32, u);
+                    tmem_wait_ld(u);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[ch * 32 + i] = __uint_as_float(u[i]);
+                }
+                const int n0 = j * C::BN;
+                const bool need_mask =
+                    (n0 + C::BN > p.Sk) || (p.causal && (n0 + C::BN - 1 > tile_row0 + off));
+                if (need_mask) {
+                    int kmax = p.Sk - 1 - n0;
+                    if (p.causal) kmax = min(kmax, row + off - n0);
+#pragma unroll
+                    for (int i = 0; i < C::BN; ++i)
+                        if (i > kmax) s[i] = kNegInf;
+                }
+                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+                for (int i = 4; i < C::BN; i += 4) {
+                    mx0 = fmaxf(mx0, s[i]);
+                    mx1 = fmaxf(mx1, s[i + 1]);
+                    mx2 = fmaxf(mx2, s[i + 2]);
+                    mx3 = fmaxf(mx3, s[i + 3]);
+                }
+                const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
+                const bool bump = m_blk > m_run + kRescaleLog2;
+                const float m_new = bump ? m_blk : m_run;
+                const float alpha = bump ? ex2_approx(m_run - m_new) : 1.0f;
+                m_run = m_new;
+                const float m_sub = (m_run == kNegInf) ? 0.f : m_run;
+
+                uint32_t pk[C::BN / 2];
+                float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+                for (int i = 0; i < C::BN / 2; ++i) {
+                    const float p0 = ex2_approx(fmaf(s[2 * i], p.scale_log2, -m_sub));
+                    const float p1 = ex2_approx(fmaf(s[2 * i + 1], p.scale_log2, -m_sub));
+                    sum0 += p0;
+                    sum1 += p1;
+                    pk[i] = pack2<kBF16>(p0, p1);
+                }
+                l_run = l_run * alpha + (sum0 + sum1);
+
+                if (j > 0) {
+                    // O of the previous block is complete before it may be rescaled and
+                    // before P of this block may be consumed.
+                    ok = mbar_wait(bar(C::kBarODone + q), (it - 1) & 1u, wc);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll
+                        for (int ch = 0; ch < C::D / 32; ++ch) {
+                            uint32_t u[32];
+                            tmem_ld_32x32b_x32(tO + ch * 32, u);
+                            tmem_wait_ld(u);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+                            tmem_st_32x32b_x32(tO + ch * 32, u);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int ch = 0; ch < C::BN / 64; ++ch) {
+                    uint32_t u[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) u[i] = pk[ch * 32 + i];
+                    tmem_st_32x32b_x32(tS + ch * 32, u);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(C::kBarPFull + q));
+                ++it;
+            }
+            if (!ok) break;
+
+            // ------------------------------------------------------------ epilogue ----
+            ok = mbar_wait(bar(C::kBarODone + q), (it - 1) & 1u, wc);
+            if (!ok) break;
+            tc_fence_after();
+            const float inv_l = (l_run > 0.f) ? 1.0f / l_run : 0.f;
+#pragma unroll
+            for (int ch = 0; ch < C::D / 32; ++ch) {
+                uint32_t u[32];
+                tmem_ld_32x32b_x32(tO + ch * 32, u);
+                tmem_wait_ld(u);
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[i] = pack2<kBF16>(__uint_as_float(u[2 * i]) * inv_l,
+                                        __uint_as_float(u[2 * i + 1]) * inv_l);
+                if (row < p.Sq) {
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        st_global_v4(orow + ch * 32 + v4 * 8, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
+                                     w[4 * v4 + 3]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(C::kBarODrained + q));
+            if (p.lse && row < p.Sq) {
+                const float lse = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.69314718055994531f
+                                                : kNegInf;
+                p.lse[((size_t)c.b * p.Hq + c.h) * p.Sq + row] = lse;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == C::kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+// Host launcher for one configuration.
+template <class C>
+fa_status launch_fwd_cfg(const FwdArgs& a, cudaStream_t stream) {
+    static int attr_bf16[64] = {0};
+    static int attr_f16[64] = {0};
+    CUtensorMap tq, tk, tv;
+    if (!encode_tmap_4d(&tq, a.q, a.bf16, a.D, a.Hq, a.Sq, a.B, C::BM) ||
+        !encode_tmap_4d(&tk, a.k, a.bf16, a.D, a.Hkv, a.Sk, a.B, C::BN) ||
+        !encode_tmap_4d(&tv, a.v, a.bf16, a.D, a.Hkv, a.Sk, a.B, C::BN))
+        return FA_ERR_CUDA;
+    FwdParams p;
+    p.B = a.B;
+    p.Sq = a.Sq;
+    p.Sk = a.Sk;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.group = a.Hq / a.Hkv;
+    p.causal = a.causal ? 1 : 0;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.num_qb = (a.Sq + C::NQ * C::BM - 1) / (C::NQ * C::BM);
+    const long long tiles = (long long)a.B * a.Hq * p.num_qb;
+    if (tiles > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    p.num_tiles = (int)tiles;
+    p.o = a.o;
+    p.lse = a.lse;
+    p.status = a.dev_status;
+    const int grid = p.num_tiles < a.num_sms ? p.num_tiles : a.num_sms;
+    auto kern = a.bf16 ? fa_fwd_kernel<C, true> : fa_fwd_kernel<C, false>;
+    if (!ensure_smem_attr((const void*)kern, C::kSmemBytes, a.bf16 ? attr_bf16 : attr_f16))
+        return FA_ERR_CUDA;
+    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace fa

@@ -1,0 +1,135 @@
+/*
+ * fa.h -- C ABI of the exact tiled attention library for NVIDIA GB300 (sm_103a).
+ *
+ * Two operations, as the source pages define them:
+ *
+ *  fa_fwd             exact attention forward, O = softmax(scale * Q K^T [+ causal mask]) V,
+ *                     plus the per-row log-sum-exp.  Page "flash-attention-v100", section
+ *                     "How to use FlashAttention" (flash_attn_func: tensors
+ *                     (batch, seqlen, nheads, headdim), grouped-query heads, default scale
+ *                     1/sqrt(headdim)); section "Changelog", "2.1: Change behavior of causal
+ *                     flag" (bottom-right aligned mask, all-masked rows give zero output);
+ *                     page "ampere_flash_attention_from_scratch" (the FlashAttention-2 forward
+ *                     that tiles Q row blocks over thread blocks and streams K/V tiles).
+ *
+ *  fa_decode_splitkv  single-token decode over a KV cache with per-sequence lengths, the KV
+ *                     range cut into chunks processed by different thread blocks, each
+ *                     writing a partial output and its log-sum-exp, then merged by a
+ *                     separate kernel.  Page "flash-attention-v100", "Changelog",
+ *                     "2.2: Optimize for inference" and flash_attn_with_kvcache
+ *                     (cache_seqlens); page "flash attention-2 github" (Flash-Decoding,
+ *                     steps 1-3).
+ *
+ * Conventions for every entry point:
+ *  - Tensors are contiguous, row-major, 16-bit (bf16 or fp16 as `dtype` says):
+ *    Q [B, Sq, Hq, D], K and V [B, Sk, Hkv, D], O [B, Sq, Hq, D]; LSE is fp32 [B, Hq, Sq].
+ *    Hq must be a multiple of Hkv; Q head h reads K/V head h / (Hq / Hkv).
+ *  - All pointers are device memory owned by the caller and must be 16-byte aligned.
+ *    The library allocates nothing on these paths; the decode workspace is sized by
+ *    fa_decode_workspace_bytes() and passed in.
+ *  - Work is enqueued on `stream` and runs asynchronously; no entry point synchronises.
+ *    Arguments are validated before anything is enqueued: a bad argument returns an error
+ *    and enqueues nothing.  FA_ERR_CUDA reports a launch failure (cudaGetLastError).
+ *  - Kernel-side waits are bounded: a wait that exceeds its limit makes the kernel unwind
+ *    and records FA_ERR_TIMEOUT, read back with fa_last_device_status().
+ *  - No C++ exception crosses this interface.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, non-positive size, Hq % Hkv != 0 */
+    FA_ERR_UNSUPPORTED = 2, /* head dim not in {64, 96, 128, 256}, unknown dtype */
+    FA_ERR_WORKSPACE = 3,   /* decode workspace missing or smaller than required */
+    FA_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed */
+    FA_ERR_TIMEOUT = 5      /* a kernel gave up on a bounded wait (see fa_last_device_status) */
+} fa_status;
+
+typedef enum { FA_BF16 = 0, FA_FP16 = 1 } fa_dtype;
+
+/*
+ * Exact attention forward (FlashAttention-2 style: Q row blocks in parallel, K/V tiles
+ * streamed, online softmax, the Sq x Sk score matrix never stored).
+ *   q     [B, Sq, Hq, D]    k, v  [B, Sk, Hkv, D]    o  [B, Sq, Hq, D]  (dtype)
+ *   lse   [B, Hq, Sq] fp32, natural log of sum_j exp(scale * q_i . k_j) over the visible
+ *         keys; -inf for a row with no visible key (whose output row is 0).  May be NULL.
+ *   scale softmax scale (the pages' default is 1/sqrt(D); the caller passes it).
+ *   causal nonzero: key j is visible to query i iff j <= i + Sk - Sq.
+ * Sizes: B, Sq, Sk, Hq, Hkv >= 1; D in {64, 96, 128, 256}; Hq % Hkv == 0.
+ * Accumulation is fp32; P is rounded to the input dtype before the P.V product; O is
+ * rounded once (round-to-nearest-even).  Deterministic: the same inputs give the same bits.
+ */
+FA_API fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Sq,
+                 int Sk, int Hq, int Hkv, int D, float scale, int causal, fa_dtype dtype,
+                 fa_stream_t stream);
+
+/*
+ * Bytes of decode workspace fa_decode_splitkv needs for these sizes and `num_splits`
+ * (the partial outputs [B, Hq, num_splits, D] fp32 and their log-sum-exps
+ * [B, Hq, num_splits] fp32, each region 256-byte aligned).  0 for invalid sizes.
+ * Host-only; needs no GPU.
+ */
+FA_API size_t fa_decode_workspace_bytes(int B, int Hq, int D, int num_splits);
+
+/*
+ * The split count fa_decode_splitkv uses when given num_splits <= 0: enough chunks that
+ * B * Hkv * num_splits work items cover the GPU several times over, with chunks of at
+ * least 256 keys.  max_kv_len is an upper bound on the KV lengths (the cache capacity
+ * Smax will do).  num_sms <= 0 queries the current device.  Returns >= 1, or -1 on an
+ * invalid argument or when no device can be queried.
+ */
+FA_API int fa_decode_default_splits(int B, int Hkv, int max_kv_len, int num_sms);
+
+/*
+ * Split-KV decode for one query token per sequence.
+ *   q        [B, 1, Hq, D]   k_cache, v_cache [B, Smax, Hkv, D]   (dtype)
+ *   kv_lens  device int32 [B], 0 <= kv_lens[b] <= Smax: sequence b attends to cache
+ *            positions [0, kv_lens[b]).  kv_lens[b] == 0 gives o = 0, lse = -inf.
+ *   o        [B, 1, Hq, D] (dtype)      lse [B, Hq] fp32 (may be NULL)
+ *   num_splits  the most chunks any sequence is cut into (<= 0: the default above).
+ *            With L = the longest kv_lens[] divided by num_splits, rounded up to a multiple
+ *            of 128, sequence b is cut into ceil(kv_lens[b] / L) chunks of L keys; every
+ *            chunk is one work item, and a second kernel merges each sequence's chunks.
+ *   workspace   device memory of at least fa_decode_workspace_bytes(B, Hq, D, num_splits)
+ *            bytes (after the default is applied); its contents need no initialisation.
+ * Sizes: B, Hq, Hkv, Smax >= 1; D == 128 or 64; Hq % Hkv == 0; Hq / Hkv <= 16.
+ * The result does not depend on num_splits beyond fp32 rounding.  Values of kv_lens
+ * outside [0, Smax] are the caller's error and are clamped on the device.
+ */
+FA_API fa_status fa_decode_splitkv(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *kv_lens, void *o, float *lse, int B, int Hq, int Hkv,
+                            int D, int Smax, float scale, int num_splits, void *workspace,
+                            size_t workspace_bytes, fa_dtype dtype, fa_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+FA_API const char *fa_status_string(fa_status s);
+
+/*
+ * Reads and clears the sticky device status word of the current device that kernels
+ * write when a bounded wait gives up (FA_ERR_TIMEOUT); FA_OK if none did.  Synchronises
+ * the current device.  FA_ERR_CUDA if the device cannot be queried.
+ */
+FA_API fa_status fa_last_device_status(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */
