@@ -1,0 +1,486 @@
+"""Benchmark: exact attention forward + split-KV decode on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  * fa_fwd on the prefill workload [B=16, S=8192, Hq=Hkv=32, D=128], bf16, non-causal
+    (the shape of the pages' largest benchmark column, page
+    "ampere_flash_attention_from_scratch", "Performance Test");
+  * fa_decode_splitkv on the decode workload (B=8, Hq=32, Hkv=8, D=128, per-sequence
+    KV lengths U[1024, 32768], Smax=32768, default split count).
+The headline value is the forward's algorithmic TFLOP/s (4*B*Hq*Sq*Sk*D per step) over
+the whole step time; the decode's HBM GB/s is reported in the "decode" object.  Inputs
+are resident in HBM before the timed region and larger than L2 (4 GiB for the forward,
+1 GiB of KV cache for decode).  Each kernel is timed with CUDA events on the stream it is
+launched on.  `e2e` repeats the step through the public API from pinned host buffers,
+host<->device copies included.  `cpu_baseline` times the CPU oracle on a bounded sample
+of the same workload on the host's cores.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 run under torch.distributed.run: each rank runs the same per-GPU workload on
+its own GPU (independent replicas, weak scaling, no data-path collective); timing takes
+the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s (bf16) and % of GB300 tensor peak; decode HBM GB/s"
+# The pages' own number for this workload (official FlashAttention-2 on an RTX 3080, fp16,
+# [16, 8192, 32, 128]: 292.02 ms), restated in this benchmark's 4*B*H*S^2*D count.
+PAGES_TFLOPS_16_8192 = 4.0 * 16 * 32 * 8192 * 8192 * 128 / 292.02e-3 / 1e12
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------ helpers ----
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Maximum of a per-rank float over all ranks (identity for a single process)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_tiled_attention_20_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when absent or
+    taken on kernel sources that have changed since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"fa_bench_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- workloads ----
+
+def make_workloads(device):
+    import torch
+
+    from exact_tiled_attention_20_gb300 import inputs
+
+    wf = inputs.PREFILL_LONG[0]
+    wd = inputs.DECODE
+    q, k, v = inputs.fwd_inputs(wf)
+    dq, dk, dv, lens = inputs.decode_inputs(wd)
+    host = dict(q=q, k=k, v=v, dq=dq, dk=dk, dv=dv, lens=lens)
+    dev = {n: t.to(device) for n, t in host.items()}
+    dev["o"] = torch.empty_like(dev["q"])
+    dev["lse"] = torch.empty((wf.B, wf.Hq, wf.Sq), dtype=torch.float32, device=device)
+    dev["do"] = torch.empty_like(dev["dq"])
+    dev["dlse"] = torch.empty((wd.B, wd.Hq), dtype=torch.float32, device=device)
+    return wf, wd, host, dev
+
+
+def decode_bytes(wd, lens) -> float:
+    """Algorithmic HBM bytes of one decode: valid K/V rows, Q, O and LSE."""
+    kv = sum(int(n) for n in lens) * wd.Hkv * wd.D * 2 * 2
+    return float(kv + wd.B * wd.Hq * wd.D * 2 * 2 + wd.B * wd.Hq * 4)
+
+
+# --------------------------------------------------------------- native arm ----
+
+def run_native(args, rank, local_rank, world):
+    import torch
+
+    import exact_tiled_attention_20_gb300 as fa
+    from exact_tiled_attention_20_gb300 import build
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    build.build_library()
+    fa.load()
+    wf, wd, host, d = make_workloads(device)
+    stream = torch.cuda.current_stream()
+    ns = fa.fa_decode_default_splits(wd.B, wd.Hkv, wd.Smax)
+    ws = torch.empty(fa.fa_decode_workspace_bytes(wd.B, wd.Hq, wd.D, ns), dtype=torch.uint8,
+                     device=device)
+
+    def step():
+        fa.fa_fwd(d["q"], d["k"], d["v"], causal=wf.causal, scale=wf.scale, out=d["o"],
+                  lse=d["lse"], stream=stream)
+        fa.fa_decode_splitkv(d["dq"], d["dk"], d["dv"], d["lens"], scale=wd.scale,
+                             num_splits=ns, workspace=ws, out=d["do"], lse=d["dlse"],
+                             stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if fa.fa_last_device_status() != 0:
+        raise RuntimeError("device status reported a kernel timeout during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        fa.fa_fwd(d["q"], d["k"], d["v"], causal=wf.causal, scale=wf.scale, out=d["o"],
+                  lse=d["lse"], stream=stream)
+        ev[i][1].record(stream)
+        fa.fa_decode_splitkv(d["dq"], d["dk"], d["dv"], d["lens"], scale=wd.scale,
+                             num_splits=ns, workspace=ws, out=d["do"], lse=d["dlse"],
+                             stream=stream)
+        ev[i][2].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    if fa.fa_last_device_status() != 0:
+        raise RuntimeError("device status reported a kernel timeout in the timed region")
+
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, device)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    dec_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    fwd_ms = max_over_ranks(fwd_ms, world, device)
+    dec_ms = max_over_ranks(dec_ms, world, device)
+    ms_per_step = total_ms / K
+    fwd_flops = wf.flops()
+    value = world * fwd_flops / (ms_per_step * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    fwd_tflops = fwd_flops / (fwd_ms * 1e-3) / 1e12
+    peak_t = float(peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"])
+    dbytes = decode_bytes(wd, host["lens"].tolist())
+    dec_gbs = dbytes / (dec_ms * 1e-3) / 1e9
+    peak_h = float(peaks["hbm_gbs"])
+    fwd_traffic = ncu_traffic("fa_fwd_kernel")
+    dec_traffic = ncu_traffic("fa_decode_split_kernel")
+
+    # ---- end to end through the public API, host buffers, copies inside the timed region
+    e2e = None
+    if args.e2e_steps > 0:
+        pin = {n: t.pin_memory() for n, t in host.items()}
+        o_h = torch.empty_like(pin["q"]).pin_memory()
+        lse_h = torch.empty(tuple(d["lse"].shape), dtype=torch.float32).pin_memory()
+        do_h = torch.empty_like(pin["dq"]).pin_memory()
+        dlse_h = torch.empty(tuple(d["dlse"].shape), dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = sum(t.numel() * t.element_size() for t in (o_h, lse_h, do_h, dlse_h))
+
+        def e2e_step():
+            for n in ("q", "k", "v", "dq", "dk", "dv", "lens"):
+                d[n].copy_(pin[n], non_blocking=True)
+            step()
+            o_h.copy_(d["o"], non_blocking=True)
+            lse_h.copy_(d["lse"], non_blocking=True)
+            do_h.copy_(d["do"], non_blocking=True)
+            dlse_h.copy_(d["dlse"], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(a0.elapsed_time(a1) / args.e2e_steps, world, device)
+        e2e = {"value": round(world * fwd_flops / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wf, host)
+
+    if rank != 0:
+        return
+    out = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": round(value / (world * PAGES_TFLOPS_16_8192), 2),
+        "vs_baseline_ref": ("official FlashAttention-2 on an RTX 3080, fp16, [16,8192,32,128], "
+                            f"{PAGES_TFLOPS_16_8192:.1f} TFLOP/s in this count (other hardware: context)"),
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": ("fa_fwd prefill [B=16,S=8192,Hq=Hkv=32,D=128] non-causal + "
+                         f"fa_decode_splitkv [B=8,Hq=32,Hkv=8,D=128,kv_len~U[1024,32768],"
+                         f"Smax=32768,num_splits={ns}]"),
+            "global_batch": wf.B * world,
+            "seq_len": wf.Sq,
+            "parallelism": "replicas" if world == 1 else f"replicas{world}",
+            "l2": "inputs larger than L2 (fwd 4 GiB, decode KV 1 GiB)",
+        },
+        "pct_of_tensor_peak": round(100.0 * fwd_tflops / peak_t, 1),
+        "roofline": {
+            "kernel": "fa_fwd_kernel",
+            "bound": "tensor",
+            "achieved": round(fwd_tflops, 1),
+            "peak": peak_t,
+            "peak_source": f"{peak_src} bf16 sustained (kernel timed inside a long step)",
+            "unit": "TFLOP/s",
+            "frac": round(fwd_tflops / peak_t, 4),
+            "frac_of_burst": round(fwd_tflops / float(peaks["bf16_tflops"]), 4),
+            "traffic": fwd_traffic,
+            "ms_per_launch": round(fwd_ms, 4),
+        },
+        "decode": {
+            "value": round(dec_gbs, 1),
+            "unit": "GB/s",
+            "ms_per_launch": round(dec_ms, 4),
+            "algorithmic_bytes": int(dbytes),
+            "roofline": {
+                "kernel": "fa_decode_split_kernel + fa_decode_combine_kernel",
+                "bound": "hbm",
+                "achieved": round(dec_gbs, 1),
+                "peak": peak_h,
+                "peak_source": f"{peak_src} copy bandwidth",
+                "unit": "GB/s",
+                "frac": round(dec_gbs / peak_h, 4),
+                "traffic": dec_traffic,
+            },
+        },
+        "e2e": e2e,
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------- CPU baseline ----
+
+def _sample_rows(wf, n_rows, seed=7):
+    import numpy as np
+
+    rng = np.random.default_rng(seed)
+    rows = np.stack([rng.integers(0, wf.B, n_rows), rng.integers(0, wf.Hq, n_rows),
+                     rng.integers(0, wf.Sq, n_rows)], axis=1)
+    return rows.astype(np.int64)
+
+
+def _row_flops(wf, rows) -> float:
+    if not wf.causal:
+        return 4.0 * wf.Sk * wf.D * len(rows)
+    return float(sum(4.0 * min(wf.Sk, int(i) + wf.Sk - wf.Sq + 1) * wf.D for i in rows[:, 2]))
+
+
+def cpu_baseline(wf, host, target_s: float = 8.0):
+    """The oracle (fp64, as it stands) on a bounded random sample of output rows of the
+    forward workload, on all host cores; reported in the same unit as the GPU number."""
+    import oracle
+
+    cores = os.cpu_count() or 1
+    probe = _sample_rows(wf, cores, seed=3)
+    t = time.perf_counter()
+    oracle.fwd(host["q"], host["k"], host["v"], scale=wf.scale, causal=wf.causal, rows=probe,
+               nthreads=cores)
+    per_batch = max(time.perf_counter() - t, 1e-3)
+    n = max(cores, int(cores * target_s / per_batch))
+    rows = _sample_rows(wf, n)
+    t = time.perf_counter()
+    oracle.fwd(host["q"], host["k"], host["v"], scale=wf.scale, causal=wf.causal, rows=rows,
+               nthreads=cores)
+    dt = time.perf_counter() - t
+    return {"value": round(_row_flops(wf, rows) / dt / 1e12, 6), "unit": "TFLOP/s",
+            "cores": cores, "kind": "oracle",
+            "sample": (f"{n} random output rows (all {wf.Sk} keys each) of the fa_fwd workload, "
+                       f"fp64, {dt:.1f} s wall")}
+
+
+# ----------------------------------------------------------- reference arm ----
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step is a bounded sample of output rows
+    of the same forward workload, timed on the host cores."""
+    if rank != 0:
+        return
+    import numpy as np  # noqa: F401
+
+    import oracle
+    from exact_tiled_attention_20_gb300 import inputs
+
+    wf = inputs.PREFILL_LONG[0]
+    q, k, v = inputs.fwd_inputs(wf)
+    cores = os.cpu_count() or 1
+    n = 2 * cores
+    for i in range(args.warmup):
+        oracle.fwd(q, k, v, scale=wf.scale, causal=wf.causal, rows=_sample_rows(wf, cores, 100 + i),
+                   nthreads=cores)
+    flops = 0.0
+    t = time.perf_counter()
+    for i in range(args.steps):
+        rows = _sample_rows(wf, n, 1000 + i)
+        oracle.fwd(q, k, v, scale=wf.scale, causal=wf.causal, rows=rows, nthreads=cores)
+        flops += _row_flops(wf, rows)
+    dt = time.perf_counter() - t
+    value = flops / dt / 1e12
+    sample = f"{n} random output rows per step of the fa_fwd workload, fp64"
+    out = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt / max(args.steps, 1) * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "fa_fwd prefill [B=16,S=8192,Hq=Hkv=32,D=128] non-causal (row sample)",
+                   "global_batch": wf.B, "seq_len": wf.Sq, "parallelism": "host threads"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_native(args, rank, local_rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

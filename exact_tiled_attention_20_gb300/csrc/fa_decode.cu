@@ -1,8 +1,579 @@
-// fa_decode.cu -- placeholder until the split-KV kernels land.
+// fa_decode.cu -- split-KV (Flash-Decoding) single-token attention for sm_103a.
+//
+// What is computed: for each sequence b and query head h, the attention of the single
+// query q[b, h] over the cached keys/values [0, kv_lens[b]) of K/V head h / (Hq / Hkv)
+// (page "flash-attention-v100", flash_attn_with_kvcache with cache_seqlens; "Changelog",
+// "2.2: Optimize for inference").  As the Flash-Decoding steps describe (page
+// "flash attention-2 github"): (1) the keys are cut into chunks, (2) each chunk's attention
+// is computed independently, writing a partial output and its log-sum-exp, (3) a separate
+// kernel merges them with the log-sum-exp weights.
+//
+// Chunking (the reading of "split the loading across thread blocks" taken here): with
+// L = ceil(max_b kv_lens[b] / num_splits) rounded up to 128, sequence b has
+// n_b = ceil(kv_lens[b] / L) chunks of L keys.  Every (b, kv head, chunk) is one work item
+// of at most L keys, so work items are nearly equal in size whatever the length mix.
+//
+// Split kernel (persistent, one CTA per SM, walking the work items):
+//  * the producer warp streams, per item, the Q rows of the query heads sharing the KV head
+//    (a 16-row box) and the item's K/V tiles of 128 keys through a 3-stage TMA ring;
+//  * the MMA warp computes S^T = K Q^T with the 128 keys of a tile as the M dimension and
+//    the query heads (padded to 16) as N, into TMEM, then O^T += V^T P^T with the 128 head
+//    dims as M (V read MN-major straight from the swizzled tile, P^T from shared memory);
+//  * four compute warps own one key (for S^T) and one head dim (for O^T) each: per tile a
+//    cross-warp max per head, exp2 with the scale folded in, a lazily rescaled O^T, and at
+//    the end of an item the division by l and the partial (o, lse) store.
+// Decode reads every K/V byte exactly once: HBM bandwidth is the roofline.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
 #include "fa_internal.h"
+#include "fa_ptx.cuh"
 
 namespace fa {
 
-fa_status launch_decode(const DecodeArgs&, cudaStream_t) { return FA_ERR_UNSUPPORTED; }
+struct DecParams {
+    int B, Hq, Hkv, group, Smax, ns;
+    float scale_log2;
+    const int32_t* kv_lens;
+    float* o_part;    // [B, Hq, ns, D]
+    float* lse_part;  // [B, Hq, ns]
+    void* o;          // [B, Hq, D]
+    float* lse;       // [B, Hq] or null
+    int q_rows;  // query-head rows per Q box (min(16, Hq)); rows past it are never read
+    int* status;
+};
+
+constexpr int kDecD = 128;
+constexpr int kDecBN = 128;  // keys per tile = MMA M
+constexpr int kDecNS = 3;
+constexpr int kDecDA = kDecD / 64;
+constexpr int kDecKVBytes = kDecBN * kDecDA * 128;  // 32 KB
+constexpr int kDecQBytes = kDecDA * 16 * 128;       // 4 KB
+constexpr int kDecPBytes = (kDecBN / 64) * 16 * 128;  // 4 KB
+constexpr int kDecMaxB = 1024;
+constexpr int kDecThreads = 192;
+constexpr int kDecProducerWarp = 4;
+constexpr int kDecMmaWarp = 5;
+constexpr int kDecTmemCols = 64;  // S^T slots at 0 and 16, O^T at 32
+
+// barrier indices
+constexpr int kDBarQFull = 0;                   // 2
+constexpr int kDBarQEmpty = kDBarQFull + 2;     // 2
+constexpr int kDBarKFull = kDBarQEmpty + 2;     // NS
+constexpr int kDBarKEmpty = kDBarKFull + kDecNS;
+constexpr int kDBarVFull = kDBarKEmpty + kDecNS;
+constexpr int kDBarVEmpty = kDBarVFull + kDecNS;
+constexpr int kDBarSFull = kDBarVEmpty + kDecNS;  // 2
+constexpr int kDBarPFull = kDBarSFull + 2;
+constexpr int kDBarODone = kDBarPFull + 1;
+constexpr int kDBarODrained = kDBarODone + 1;
+constexpr int kDBarFinal = kDBarODrained + 1;
+constexpr int kDNumBars = kDBarFinal + 1;
+
+struct DecSmemTail {
+    uint64_t bars[kDNumBars];
+    float red[2][4][16];   // per-tile cross-warp max, double-buffered
+    float lred[4][16];     // end-of-item cross-warp sums
+    int lens[kDecMaxB];
+    int prefix[kDecMaxB + 1];  // exclusive prefix of n_b * Hkv
+    int warp_sums[4];
+    int max_len;
+    int chunk;        // L
+    int total_items;
+    uint32_t tmem_slot;
+    int abort_flag;
+};
+
+constexpr int kDecTileBytes = 2 * kDecNS * kDecKVBytes + 2 * kDecQBytes + kDecPBytes;
+constexpr int kDecSmemBytes = 1024 + kDecTileBytes + (int)sizeof(DecSmemTail);
+static_assert(kDecSmemBytes <= 232448, "decode shared memory budget");
+
+struct DecItem {
+    int b, hk, c, k0, k1, ntiles;
+};
+
+__device__ __forceinline__ DecItem decode_item(const DecSmemTail& t, int B, int Hkv, int idx) {
+    int lo = 0, hi = B;  // largest b with prefix[b] <= idx
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (t.prefix[mid] <= idx) lo = mid; else hi = mid;
+    }
+    DecItem it;
+    it.b = lo;
+    const int nb = (t.prefix[lo + 1] - t.prefix[lo]) / Hkv;
+    const int r = idx - t.prefix[lo];
+    it.hk = r / nb;
+    it.c = r % nb;
+    it.k0 = it.c * t.chunk;
+    it.k1 = min(it.k0 + t.chunk, t.lens[lo]);
+    it.ntiles = (it.k1 - it.k0 + kDecBN - 1) / kDecBN;
+    return it;
+}
+
+// Shared-memory byte address of P^T[h][key] in the 128-byte-swizzled K-major layout of a
+// 16-row x 128-key operand (two 64-key atoms of 16 rows x 128 bytes).
+__device__ __forceinline__ uint32_t pt_addr(uint32_t sP, int h, int key) {
+    const uint32_t byte = (uint32_t)(key & 63) * 2u;
+    return sP + (uint32_t)(key >> 6) * 2048u + (uint32_t)h * 128u +
+           ((((byte >> 4) ^ (uint32_t)(h & 7)) << 4) | (byte & 15u));
+}
+
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+template <bool kBF16>
+__device__ __forceinline__ uint16_t to16(float x) {
+    uint32_t w = pack2<kBF16>(x, 0.f);
+    return (uint16_t)(w & 0xffffu);
+}
+
+template <int GMAX, bool kBF16>
+__global__ void __launch_bounds__(kDecThreads, 1)
+    fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v, const DecParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t base = (raw_u32 + 1023u) & ~1023u;
+    uint8_t* base_gen = smem_raw + (base - raw_u32);
+    const uint32_t sK = base;
+    const uint32_t sV = sK + kDecNS * kDecKVBytes;
+    const uint32_t sQ = sV + kDecNS * kDecKVBytes;
+    const uint32_t sP = sQ + 2 * kDecQBytes;
+    DecSmemTail& T = *reinterpret_cast<DecSmemTail*>(base_gen + kDecTileBytes);
+    auto bar = [&](int i) -> uint32_t { return smem_u32(&T.bars[i]); };
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const WaitCtx wc{&T.abort_flag, p.status};
+
+    // ---- setup: barriers, TMEM, and the work-item table from kv_lens
+    if (tid == 0) {
+        for (int i = 0; i < kDNumBars; ++i)
+            mbar_init(bar(i), (i == kDBarPFull || i == kDBarODrained) ? 128u : 1u);
+        T.abort_flag = 0;
+        T.max_len = 0;
+        fence_mbar_init();
+    }
+    if (warp == kDecMmaWarp) {
+        tmem_alloc(smem_u32(&T.tmem_slot), kDecTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kDecProducerWarp && lane == 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    // P^T rows past the group stay zero for the whole kernel.
+    for (int i = tid; i < kDecPBytes / 4; i += kDecThreads)
+        reinterpret_cast<uint32_t*>(base_gen + (sP - base))[i] = 0u;
+    fence_proxy_async_smem();
+    __syncthreads();
+    for (int b = tid; b < p.B; b += kDecThreads) {
+        const int len = min(max(p.kv_lens[b], 0), p.Smax);
+        T.lens[b] = len;
+        atomicMax(&T.max_len, len);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const int per = (T.max_len + p.ns - 1) / p.ns;
+        T.chunk = max(kDecBN, (per + kDecBN - 1) / kDecBN * kDecBN);
+    }
+    __syncthreads();
+    {
+        // exclusive scan of n_b * Hkv over b, 128 threads x up to 8 entries each
+        const int per_t = (p.B + 127) / 128;
+        int local = 0;
+        if (tid < 128) {
+            for (int i = 0; i < per_t; ++i) {
+                const int b = tid * per_t + i;
+                if (b < p.B) local += (T.lens[b] + T.chunk - 1) / T.chunk * p.Hkv;
+            }
+        }
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (tid < 128 && lane == 31) T.warp_sums[warp] = incl;
+        __syncthreads();
+        if (tid < 128) {
+            int run = incl - local;
+            for (int w = 0; w < warp; ++w) run += T.warp_sums[w];
+            for (int i = 0; i < per_t; ++i) {
+                const int b = tid * per_t + i;
+                if (b < p.B) {
+                    T.prefix[b] = run;
+                    run += (T.lens[b] + T.chunk - 1) / T.chunk * p.Hkv;
+                }
+            }
+            if (tid == 127) T.total_items = run;
+        }
+        if (tid == 0 && p.B <= 0) T.total_items = 0;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) T.prefix[p.B] = T.total_items;
+    __syncthreads();
+    const uint32_t tmem = T.tmem_slot;
+    const int total = T.total_items;
+
+    if (warp == kDecProducerWarp) {
+        // -------------------------------------------------------------- producer ----
+        if (lane == 0) {
+            uint32_t kv_it = 0, icount = 0;
+            bool ok = true;
+            for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
+                const DecItem it = decode_item(T, p.B, p.Hkv, idx);
+                const uint32_t qs = icount & 1u;
+                ok = mbar_wait(bar(kDBarQEmpty + qs), ((icount >> 1) & 1u) ^ 1u, wc);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar(kDBarQFull + qs), kDecDA * p.q_rows * 128);
+                for (int a = 0; a < kDecDA; ++a)
+                    tma_load_4d(sQ + qs * kDecQBytes + a * 2048, &tm_q, bar(kDBarQFull + qs), a * 64,
+                                it.hk * p.group, 0, it.b);
+                for (int j = 0; j < it.ntiles && ok; ++j) {
+                    const uint32_t st = kv_it % kDecNS;
+                    const uint32_t ph = ((kv_it / kDecNS) & 1u) ^ 1u;
+                    const int row = it.k0 + j * kDecBN;
+                    ok = mbar_wait(bar(kDBarKEmpty + st), ph, wc);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(kDBarKFull + st), kDecKVBytes);
+                    for (int a = 0; a < kDecDA; ++a)
+                        tma_load_4d(sK + st * kDecKVBytes + a * (kDecBN * 128), &tm_k,
+                                    bar(kDBarKFull + st), a * 64, it.hk, row, it.b);
+                    ok = mbar_wait(bar(kDBarVEmpty + st), ph, wc);
+                    if (!ok) {
+                        mbar_wait_drain(bar(kDBarKFull + st), (kv_it / kDecNS) & 1u);
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(kDBarVFull + st), kDecKVBytes);
+                    for (int a = 0; a < kDecDA; ++a)
+                        tma_load_4d(sV + st * kDecKVBytes + a * (kDecBN * 128), &tm_v,
+                                    bar(kDBarVFull + st), a * 64, it.hk, row, it.b);
+                    ++kv_it;
+                }
+                ++icount;
+            }
+            for (uint32_t d = 0; d < (uint32_t)kDecNS && d < kv_it; ++d) {
+                const uint32_t last = kv_it - 1 - d;
+                mbar_wait_drain(bar(kDBarKFull + last % kDecNS), (last / kDecNS) & 1u);
+                mbar_wait_drain(bar(kDBarVFull + last % kDecNS), (last / kDecNS) & 1u);
+            }
+            for (uint32_t d = 0; d < 2u && d < icount; ++d) {
+                const uint32_t last = icount - 1 - d;
+                mbar_wait_drain(bar(kDBarQFull + (last & 1u)), (last >> 1) & 1u);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kDecMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer ----
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = make_idesc_f16(128, 16, kBF16, false, false);
+            constexpr uint32_t idesc_o = make_idesc_f16(128, 16, kBF16, true, false);
+            uint32_t kv_it = 0, icount = 0, it_s = 0;
+            bool ok = true;
+            auto issue_s = [&](uint32_t qs, uint32_t kst, uint32_t slot) {
+#pragma unroll
+                for (int kk = 0; kk < kDecD / 16; ++kk) {
+                    const uint32_t a_addr = sK + kst * kDecKVBytes + (kk >> 2) * (kDecBN * 128) + (kk & 3) * 32;
+                    const uint32_t b_addr = sQ + qs * kDecQBytes + (kk >> 2) * 2048 + (kk & 3) * 32;
+                    umma_ss(tmem + slot * 16, make_sdesc_sw128(a_addr, 16, 1024),
+                            make_sdesc_sw128(b_addr, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](uint32_t vst, bool acc) {
+#pragma unroll
+                for (int kk = 0; kk < kDecBN / 16; ++kk) {
+                    const uint32_t a_addr = sV + vst * kDecKVBytes + kk * (16 * 128);
+                    const uint32_t b_addr = sP + (kk >> 2) * 2048 + (kk & 3) * 32;
+                    umma_ss(tmem + 32, make_sdesc_sw128(a_addr, kDecBN * 128, 1024),
+                            make_sdesc_sw128(b_addr, 16, 1024), idesc_o, (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
+                const DecItem item = decode_item(T, p.B, p.Hkv, idx);
+                const int n = item.ntiles;
+                const uint32_t qs = icount & 1u;
+                ok = mbar_wait(bar(kDBarQFull + qs), (icount >> 1) & 1u, wc);
+                if (!ok) break;
+                {
+                    const uint32_t st = kv_it % kDecNS;
+                    ok = mbar_wait(bar(kDBarKFull + st), (kv_it / kDecNS) & 1u, wc);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(qs, st, it_s & 1u);
+                    umma_commit(bar(kDBarSFull + (it_s & 1u)));
+                    umma_commit(bar(kDBarKEmpty + st));
+                    if (n == 1) umma_commit(bar(kDBarQEmpty + qs));
+                }
+                for (int j = 0; j < n && ok; ++j) {
+                    const uint32_t cur = kv_it + j;
+                    const uint32_t st = cur % kDecNS;
+                    if (j + 1 < n) {
+                        const uint32_t nst = (cur + 1) % kDecNS;
+                        ok = mbar_wait(bar(kDBarKFull + nst), ((cur + 1) / kDecNS) & 1u, wc);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(qs, nst, (it_s + 1) & 1u);
+                        umma_commit(bar(kDBarSFull + ((it_s + 1) & 1u)));
+                        umma_commit(bar(kDBarKEmpty + nst));
+                        if (j + 2 == n) umma_commit(bar(kDBarQEmpty + qs));
+                    }
+                    ok = mbar_wait(bar(kDBarPFull), it_s & 1u, wc);
+                    if (ok && j == 0 && icount > 0)
+                        ok = mbar_wait(bar(kDBarODrained), (icount - 1) & 1u, wc);
+                    if (ok) ok = mbar_wait(bar(kDBarVFull + st), (cur / kDecNS) & 1u, wc);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(st, j > 0);
+                    umma_commit(bar(kDBarODone));
+                    umma_commit(bar(kDBarVEmpty + st));
+                    ++it_s;
+                }
+                kv_it += n;
+                ++icount;
+            }
+            umma_commit(bar(kDBarFinal));
+            mbar_wait_drain(bar(kDBarFinal), 0);
+        }
+        __syncwarp();
+    } else {
+        // --------------------------------------------------------- compute warps ----
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const float kNegInf = -__int_as_float(0x7f800000);
+        const int g = p.group;
+        uint32_t it_s = 0;
+        bool ok = true;
+        for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
+            const DecItem item = decode_item(T, p.B, p.Hkv, idx);
+            float m_run[GMAX], l_part[GMAX];
+#pragma unroll
+            for (int h = 0; h < GMAX; ++h) {
+                m_run[h] = kNegInf;
+                l_part[h] = 0.f;
+            }
+            for (int j = 0; j < item.ntiles; ++j) {
+                const uint32_t slot = it_s & 1u;
+                ok = mbar_wait(bar(kDBarSFull + slot), (it_s >> 1) & 1u, wc);
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t u[16];
+                tmem_ld_32x32b_x16(lane_base + slot * 16, u);
+                tmem_wait_ld(u);
+                const bool valid = item.k0 + j * kDecBN + tid < item.k1;
+                float sv[GMAX];
+#pragma unroll
+                for (int h = 0; h < GMAX; ++h) {
+                    sv[h] = (valid && h < g) ? __uint_as_float(u[h]) : kNegInf;
+                    float m = sv[h];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    if (lane == 0) T.red[j & 1][warp][h] = m;
+                }
+                named_bar_sync(1, 128);
+                float alpha[GMAX], msub[GMAX];
+                bool any_rescale = false;
+#pragma unroll
+                for (int h = 0; h < GMAX; ++h) {
+                    const float mb = fmaxf(fmaxf(T.red[j & 1][0][h], T.red[j & 1][1][h]),
+                                           fmaxf(T.red[j & 1][2][h], T.red[j & 1][3][h])) *
+                                     p.scale_log2;
+                    const bool bump = mb > m_run[h] + 8.0f;
+                    const float mn = bump ? mb : m_run[h];
+                    alpha[h] = bump ? ex2_approx(m_run[h] - mn) : 1.0f;
+                    any_rescale |= bump;
+                    m_run[h] = mn;
+                    msub[h] = (mn == kNegInf) ? 0.f : mn;
+                }
+                float pv[GMAX];
+#pragma unroll
+                for (int h = 0; h < GMAX; ++h) {
+                    pv[h] = ex2_approx(fmaf(sv[h], p.scale_log2, -msub[h]));
+                    l_part[h] = l_part[h] * alpha[h] + pv[h];
+                }
+                if (j > 0) {
+                    // the previous P.V has finished reading P^T and may now be rescaled
+                    ok = mbar_wait(bar(kDBarODone), (it_s - 1) & 1u, wc);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (any_rescale) {  // uniform: every thread saw the same maxima
+                        uint32_t ov[16];
+                        tmem_ld_32x32b_x16(lane_base + 32, ov);
+                        tmem_wait_ld(ov);
+#pragma unroll
+                        for (int h = 0; h < GMAX; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
+                        tmem_st_32x32b_x16(lane_base + 32, ov);
+                        tmem_wait_st();
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < GMAX; ++h) st_shared_u16(pt_addr(sP, h, tid), to16<kBF16>(pv[h]));
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(bar(kDBarPFull));
+                ++it_s;
+            }
+            if (!ok) break;
+            // ---- end of item: O^T / l -> partial output, log-sum-exp per head
+            ok = mbar_wait(bar(kDBarODone), (it_s - 1) & 1u, wc);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t ov[16];
+            tmem_ld_32x32b_x16(lane_base + 32, ov);
+            tmem_wait_ld(ov);
+            tc_fence_before();
+            mbar_arrive(bar(kDBarODrained));
+#pragma unroll
+            for (int h = 0; h < GMAX; ++h) {
+                float s = l_part[h];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                if (lane == 0) T.lred[warp][h] = s;
+            }
+            named_bar_sync(1, 128);
+            const size_t row0 = ((size_t)item.b * p.Hq + (size_t)item.hk * g) * p.ns + item.c;
+#pragma unroll
+            for (int h = 0; h < GMAX; ++h) {
+                const float lt = (T.lred[0][h] + T.lred[1][h]) + (T.lred[2][h] + T.lred[3][h]);
+                if (h < g) {
+                    const size_t row = row0 + (size_t)h * p.ns;
+                    p.o_part[row * kDecD + tid] = lt > 0.f ? __uint_as_float(ov[h]) / lt : 0.f;
+                    if (tid == 0)
+                        p.lse_part[row] =
+                            lt > 0.f ? (m_run[h] + lg2_approx(lt)) * 0.69314718055994531f : kNegInf;
+                }
+            }
+            // lred is rewritten only after the next item's per-tile barriers
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kDecMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kDecTmemCols);
+    }
+}
+
+// Merge kernel: one warp per (b, query head); lane l owns head dims 4l .. 4l+3.
+template <bool kBF16>
+__global__ void __launch_bounds__(128)
+    fa_decode_combine_kernel(const DecParams p) {
+    __shared__ int s_max_len;
+    if (threadIdx.x == 0) s_max_len = 0;
+    __syncthreads();
+    for (int b = threadIdx.x; b < p.B; b += blockDim.x)
+        atomicMax(&s_max_len, min(max(p.kv_lens[b], 0), p.Smax));
+    __syncthreads();
+    const int per = (s_max_len + p.ns - 1) / p.ns;
+    const int L = max(kDecBN, (per + kDecBN - 1) / kDecBN * kDecBN);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.x * 4 + warp;
+    if (bh >= p.B * p.Hq) return;
+    const int b = bh / p.Hq;
+    const int len = min(max(p.kv_lens[b], 0), p.Smax);
+    const int n = (len + L - 1) / L;
+    const float kNegInf = -__int_as_float(0x7f800000);
+    const float kLog2e = 1.4426950408889634f;
+    const float* lrow = p.lse_part + (size_t)bh * p.ns;
+    const float* orow = p.o_part + (size_t)bh * p.ns * kDecD;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float lse = kNegInf;
+    if (n > 0) {
+        float m = kNegInf;
+        for (int c = lane; c < n; c += 32) m = fmaxf(m, lrow[c]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float s = 0.f;
+        for (int c = lane; c < n; c += 32) s += ex2_approx((lrow[c] - m) * kLog2e);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        for (int c = 0; c < n; ++c) {
+            const float w = ex2_approx((lrow[c] - m) * kLog2e);
+            const float4 v = *reinterpret_cast<const float4*>(orow + (size_t)c * kDecD + lane * 4);
+            acc[0] = fmaf(w, v.x, acc[0]);
+            acc[1] = fmaf(w, v.y, acc[1]);
+            acc[2] = fmaf(w, v.z, acc[2]);
+            acc[3] = fmaf(w, v.w, acc[3]);
+        }
+        const float inv = 1.0f / s;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] *= inv;
+        lse = m + lg2_approx(s) * 0.69314718055994531f;
+    }
+    uint16_t* out = reinterpret_cast<uint16_t*>(p.o) + (size_t)bh * kDecD + lane * 4;
+    const uint32_t w0 = pack2<kBF16>(acc[0], acc[1]);
+    const uint32_t w1 = pack2<kBF16>(acc[2], acc[3]);
+    asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(out), "r"(w0), "r"(w1) : "memory");
+    if (p.lse && lane == 0) p.lse[bh] = lse;
+}
+
+template <int GMAX, bool kBF16>
+static fa_status launch_split(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const DecParams& p, int grid, cudaStream_t s) {
+    static int attr[64] = {0};
+    auto kern = fa_decode_split_kernel<GMAX, kBF16>;
+    if (!ensure_smem_attr((const void*)kern, kDecSmemBytes, attr)) return FA_ERR_CUDA;
+    kern<<<grid, kDecThreads, kDecSmemBytes, s>>>(tq, tk, tv, p);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
+    if (a.D != kDecD) return FA_ERR_UNSUPPORTED;
+    if (a.B > kDecMaxB) return FA_ERR_UNSUPPORTED;
+    const int g = a.Hq / a.Hkv;
+    CUtensorMap tq, tk, tv;
+    const int q_rows = a.Hq < 16 ? a.Hq : 16;
+    if (!encode_tmap_4d_box(&tq, a.q, a.bf16, a.D, a.Hq, 1, a.B, q_rows, 1) ||
+        !encode_tmap_4d(&tk, a.k_cache, a.bf16, a.D, a.Hkv, a.Smax, a.B, kDecBN) ||
+        !encode_tmap_4d(&tv, a.v_cache, a.bf16, a.D, a.Hkv, a.Smax, a.B, kDecBN))
+        return FA_ERR_CUDA;
+    DecParams p;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.group = g;
+    p.Smax = a.Smax;
+    p.ns = a.num_splits;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.kv_lens = a.kv_lens;
+    p.o_part = a.o_part;
+    p.lse_part = a.lse_part;
+    p.o = a.o;
+    p.lse = a.lse;
+    p.status = a.dev_status;
+    p.q_rows = q_rows;
+    const long long items_max = (long long)a.B * a.Hkv * a.num_splits;
+    const int grid = (int)(items_max < a.num_sms ? items_max : a.num_sms);
+    fa_status st;
+    if (g <= 4)
+        st = a.bf16 ? launch_split<4, true>(tq, tk, tv, p, grid, s) : launch_split<4, false>(tq, tk, tv, p, grid, s);
+    else if (g <= 8)
+        st = a.bf16 ? launch_split<8, true>(tq, tk, tv, p, grid, s) : launch_split<8, false>(tq, tk, tv, p, grid, s);
+    else
+        st = a.bf16 ? launch_split<16, true>(tq, tk, tv, p, grid, s) : launch_split<16, false>(tq, tk, tv, p, grid, s);
+    if (st != FA_OK) return st;
+    const int cgrid = (a.B * a.Hq + 3) / 4;
+    if (a.bf16)
+        fa_decode_combine_kernel<true><<<cgrid, 128, 0, s>>>(p);
+    else
+        fa_decode_combine_kernel<false><<<cgrid, 128, 0, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
 
 }  // namespace fa
