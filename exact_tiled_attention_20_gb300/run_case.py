@@ -1,0 +1,63 @@
+"""Runs one forward or decode case a few times -- a small, self-contained driver for
+profiling a single kernel (e.g. under ncu) on inputs resident on the GPU.
+
+  python -m exact_tiled_attention_20_gb300.run_case fwd B S Hq Hkv D causal [iters]
+  python -m exact_tiled_attention_20_gb300.run_case decode B Hq Hkv D Smax [iters]
+
+Inputs are drawn on the device from a fixed seed (values do not matter for profiling);
+the script prints the mean time per call from CUDA events.
+"""
+from __future__ import annotations
+
+import sys
+
+import torch
+
+from . import _lib as fa
+from . import build
+
+
+def main(argv):
+    build.build_library()
+    fa.load()
+    dev = torch.device("cuda:0")
+    g = torch.Generator(device=dev).manual_seed(0)
+    kind = argv[0]
+    if kind == "fwd":
+        B, S, Hq, Hkv, D, causal = (int(x) for x in argv[1:7])
+        iters = int(argv[7]) if len(argv) > 7 else 3
+        q = torch.randn(B, S, Hq, D, device=dev, generator=g, dtype=torch.bfloat16)
+        k = torch.randn(B, S, Hkv, D, device=dev, generator=g, dtype=torch.bfloat16)
+        v = torch.randn(B, S, Hkv, D, device=dev, generator=g, dtype=torch.bfloat16)
+        o = torch.empty_like(q)
+        lse = torch.empty(B, Hq, S, device=dev, dtype=torch.float32)
+        call = lambda: fa.fa_fwd(q, k, v, causal=bool(causal), out=o, lse=lse)  # noqa: E731
+    elif kind == "decode":
+        B, Hq, Hkv, D, Smax = (int(x) for x in argv[1:6])
+        iters = int(argv[6]) if len(argv) > 6 else 3
+        q = torch.randn(B, 1, Hq, D, device=dev, generator=g, dtype=torch.bfloat16)
+        kc = torch.randn(B, Smax, Hkv, D, device=dev, generator=g, dtype=torch.bfloat16)
+        vc = torch.randn(B, Smax, Hkv, D, device=dev, generator=g, dtype=torch.bfloat16)
+        lens = torch.randint(Smax // 32, Smax + 1, (B,), device=dev, generator=g, dtype=torch.int32)
+        ns = fa.fa_decode_default_splits(B, Hkv, Smax)
+        ws = torch.empty(fa.fa_decode_workspace_bytes(B, Hq, D, ns), dtype=torch.uint8, device=dev)
+        o = torch.empty_like(q)
+        call = lambda: fa.fa_decode_splitkv(q, kc, vc, lens, num_splits=ns, workspace=ws, out=o)  # noqa: E731
+    else:
+        raise SystemExit(__doc__)
+    call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    st = fa.fa_last_device_status()
+    print(f"{kind} {' '.join(argv[1:])}: {e0.elapsed_time(e1) / iters:.4f} ms/call, status {st}")
+    if st != 0:
+        raise SystemExit(1)
+
+
+if __name__ == "__main__":
+    main(sys.argv[1:])
