@@ -183,3 +183,39 @@ def fa_decode_splitkv(q, k_cache, v_cache, kv_lens, scale: float | None = None,
     if st != FA_OK:
         raise FaError(st, "fa_decode_splitkv")
     return out, lse
+
+
+_noalloc_declared = False
+
+
+def fa_decode_splitkv_noalloc(q, k_cache, v_cache, kv_lens, scale: float | None = None,
+                              num_splits: int = 0, out=None, lse=None, stream=None):
+    """fa_decode_splitkv_noalloc: split-KV decode without a caller workspace, for callers
+    that cannot allocate device memory (the partials go to a fixed scratch array inside
+    the library; see include/fa.h for its size limit and sharing rules).  Output tensors
+    must be given or are created here with PyTorch."""
+    global _noalloc_declared
+    lib = load()
+    if not _noalloc_declared:
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.fa_decode_splitkv_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, I, I, P]
+        lib.fa_decode_splitkv_noalloc.restype = I
+        _noalloc_declared = True
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _check_cuda(name, t, q.dtype)
+    _check_cuda("kv_lens", kv_lens, torch.int32)
+    B, _, Hq, D = q.shape
+    _, Smax, Hkv, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        st = lib.fa_decode_splitkv_noalloc(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                           kv_lens.data_ptr(), out.data_ptr(), lse.data_ptr(), B,
+                                           Hq, Hkv, D, Smax, sc, int(num_splits), _DTYPE[q.dtype],
+                                           _stream_handle(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_decode_splitkv_noalloc")
+    return out, lse

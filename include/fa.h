@@ -118,6 +118,33 @@ FA_API fa_status fa_decode_splitkv(const void *q, const void *k_cache, const voi
                             int D, int Smax, float scale, int num_splits, void *workspace,
                             size_t workspace_bytes, fa_dtype dtype, fa_stream_t stream);
 
+/*
+ * Split-KV decode for callers that cannot allocate device memory -- for example a plugin
+ * running inside a host runtime that owns every device allocation, or a latency-critical
+ * serving loop that must never call cudaMalloc (which may synchronise the device).  The
+ * source pages have no counterpart to this entry point; it exists for those callers.
+ *
+ * Same arguments and results as fa_decode_splitkv, minus the workspace: the partial
+ * results go to a fixed scratch array of FA_DECODE_NOALLOC_SCRATCH_BYTES that lives in
+ * the library's device image (every GPU that loads the library holds it until the process
+ * exits).  The call allocates nothing and calls no allocating routine.
+ *  - Limit: sizes whose workspace, fa_decode_workspace_bytes(B, Hq, D, num_splits) after
+ *    the default split count is applied, exceeds FA_DECODE_NOALLOC_SCRATCH_BYTES are
+ *    rejected with FA_ERR_WORKSPACE before anything is enqueued.
+ *  - Set-up: the first call on each device (with that device current) looks up the
+ *    array's device address once; make that first call before any stream capture.
+ *  - Sharing: every call on a device uses the same array and leaves its contents behind.
+ *    Nothing in it needs to start at zero (each call writes every partial it reads), but
+ *    calls whose kernels overlap on the GPU (e.g. on two streams at once) race on it.
+ */
+#define FA_DECODE_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+
+FA_API fa_status fa_decode_splitkv_noalloc(const void *q, const void *k_cache,
+                                           const void *v_cache, const int32_t *kv_lens, void *o,
+                                           float *lse, int B, int Hq, int Hkv, int D, int Smax,
+                                           float scale, int num_splits, fa_dtype dtype,
+                                           fa_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 FA_API const char *fa_status_string(fa_status s);
 
