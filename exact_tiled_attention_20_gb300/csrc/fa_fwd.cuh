@@ -61,6 +61,9 @@ struct FwdConfig {
     static_assert(kOCol0 + NQ * D <= kTmemCols, "TMEM budget");
     static_assert(D % 32 == 0 && BN % 64 == 0, "tile shape");
     static constexpr int kThreads = 128 * NQ + 64;
+    // O-done is signalled after every P.V when S is issued ahead of P.V (NQ == 1), and
+    // only after a tile's last P.V otherwise.
+    static constexpr bool kOPerIter = (NQ == 1);
     static constexpr int kProducerWarp = 4 * NQ;
     static constexpr int kMmaWarp = 4 * NQ + 1;
     // barrier indices
@@ -125,6 +128,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const WaitCtx wc{abort_flag, p.status};
+    constexpr bool kOPerIter = C::kOPerIter;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
@@ -209,27 +213,34 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             uint32_t kv_it = 0, tcount = 0, it = 0;
             bool ok = true;
 
+            // Descriptors are built once; stepping K by 16 elements only advances the
+            // start-address field, so each MMA issues with a constant 64-bit add.  The
+            // issuing thread is on the critical path: keep this loop lean.
+            const uint64_t dq0 = make_sdesc_sw128(sQ, 16, 1024);
+            const uint64_t dk0 = make_sdesc_sw128(sK, 16, 1024);
+            const uint64_t dv0 = make_sdesc_sw128(sV, C::BN * 128, 1024);
             auto issue_s = [&](int q, uint32_t kst, uint32_t slot) {
                 const uint32_t d = tmem + slot * C::BN;
+                const uint64_t a = dq0 + (uint64_t)((q * C::kQBytes) >> 4);
+                const uint64_t b = dk0 + (uint64_t)((kst * C::kKVBytes) >> 4);
+                umma_ss_imm<false>(d, a, b, idesc_s);
 #pragma unroll
-                for (int kk = 0; kk < C::D / 16; ++kk) {
-                    const uint32_t a_addr =
-                        sQ + q * C::kQBytes + (kk >> 2) * (C::BM * 128) + (kk & 3) * 32;
-                    const uint32_t b_addr =
-                        sK + kst * C::kKVBytes + (kk >> 2) * (C::BN * 128) + (kk & 3) * 32;
-                    umma_ss(d, make_sdesc_sw128(a_addr, 16, 1024), make_sdesc_sw128(b_addr, 16, 1024),
-                            idesc_s, kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 1; kk < C::D / 16; ++kk)
+                    umma_ss_imm<true>(d, a + (uint64_t)(((kk >> 2) * (C::BM * 128) + (kk & 3) * 32) >> 4),
+                                      b + (uint64_t)(((kk >> 2) * (C::BN * 128) + (kk & 3) * 32) >> 4),
+                                      idesc_s);
             };
             auto issue_pv = [&](int q, uint32_t vst, uint32_t slot, bool acc) {
                 const uint32_t d = tmem + C::kOCol0 + q * C::D;
+                const uint32_t a = tmem + slot * C::BN;
+                const uint64_t b = dv0 + (uint64_t)((vst * C::kKVBytes) >> 4);
+                if (acc)
+                    umma_ts_imm<true>(d, a, b, idesc_o);
+                else
+                    umma_ts_imm<false>(d, a, b, idesc_o);
 #pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk) {
-                    const uint32_t a_tmem = tmem + slot * C::BN + kk * 8;
-                    const uint32_t b_addr = sV + vst * C::kKVBytes + kk * (16 * 128);
-                    umma_ts(d, a_tmem, make_sdesc_sw128(b_addr, C::BN * 128, 1024), idesc_o,
-                            (acc || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 1; kk < C::BN / 16; ++kk)
+                    umma_ts_imm<true>(d, a + kk * 8, b + (uint64_t)((kk * (16 * 128)) >> 4), idesc_o);
             };
             auto slot_of = [&](int q, uint32_t iter) -> uint32_t {
                 return C::NQ == 1 ? (iter & 1u) : (uint32_t)q;
@@ -277,7 +288,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                         if (!ok) break;
                         tc_fence_after();
                         issue_pv(q, st, slot_of(q, it), j > 0);
-                        umma_commit(bar(C::kBarODone + q));
+                        if (kOPerIter || j + 1 == n) umma_commit(bar(C::kBarODone + q));
                         if (C::NQ > 1 && more) {
                             if (q == 0) {
                                 ok = mbar_wait(bar(C::kBarKFull + nst), ((cur + 1) / C::NS) & 1u, wc);
@@ -311,8 +322,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const uint32_t tO = lane_base + C::kOCol0 + q * C::D;
         const float kNegInf = -__int_as_float(0x7f800000);
         constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
+        constexpr int kSC = C::BN / 32;        // 32-column chunks of S per block
         const int off = p.Sk - p.Sq;           // bottom-right causal alignment
-        uint32_t it = 0;
+        const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
+        uint32_t it = 0, tcount = 0;
         bool ok = true;
 
         for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
@@ -329,7 +342,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 continue;
             }
             float m_run = kNegInf;  // running max, log2 units (raw score * scale * log2 e)
-            float l_run = 0.f;
+            uint64_t l2 = f2_pack(0.f, 0.f);  // running sum, two interleaved partial sums
             const int tile_row0 = c.m0 + q * C::BM;
 
             for (int j = 0; j < c.n_kv; ++j) {
@@ -339,15 +352,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t tS = lane_base + slot * C::BN;
-                float s[C::BN];
+                // All chunks of S are loaded before a single wait.
+                uint32_t u[kSC][32];
 #pragma unroll
-                for (int ch = 0; ch < C::BN / 32; ++ch) {
-                    uint32_t u[32];
-                    tmem_ld_32x32b_x32(tS + ch * 32, u);
-                    tmem_wait_ld(u);
+                for (int ch = 0; ch < kSC; ++ch) tmem_ld_32x32b_x32(tS + ch * 32, u[ch]);
+                tmem_wait_ld(u[0]);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) s[ch * 32 + i] = __uint_as_float(u[i]);
-                }
+                for (int ch = 1; ch < kSC; ++ch) reg_fence(u[ch]);
+
                 const int n0 = j * C::BN;
                 const bool need_mask =
                     (n0 + C::BN > p.Sk) || (p.causal && (n0 + C::BN - 1 > tile_row0 + off));
@@ -355,60 +367,71 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     int kmax = p.Sk - 1 - n0;
                     if (p.causal) kmax = min(kmax, row + off - n0);
 #pragma unroll
-                    for (int i = 0; i < C::BN; ++i)
-                        if (i > kmax) s[i] = kNegInf;
-                }
-                float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+                    for (int ch = 0; ch < kSC; ++ch)
 #pragma unroll
-                for (int i = 4; i < C::BN; i += 4) {
-                    mx0 = fmaxf(mx0, s[i]);
-                    mx1 = fmaxf(mx1, s[i + 1]);
-                    mx2 = fmaxf(mx2, s[i + 2]);
-                    mx3 = fmaxf(mx3, s[i + 3]);
+                        for (int i = 0; i < 32; ++i)
+                            if (ch * 32 + i > kmax) u[ch][i] = 0xff800000u;  // -inf
                 }
-                const float m_blk = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
+                // Row max over the BN scores: four independent chains of 3-input maxima.
+                auto sv = [&](int k) -> float { return __uint_as_float(u[k >> 5][k & 31]); };
+                float mx[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) mx[k] = sv(k);
+#pragma unroll
+                for (int k = 4; k + 8 <= C::BN; k += 8)
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) mx[c4] = max3f(mx[c4], sv(k + c4), sv(k + c4 + 4));
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) mx[c4] = fmaxf(mx[c4], sv(C::BN - 4 + c4));
+                const float m_blk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
                 const bool bump = m_blk > m_run + kRescaleLog2;
                 const float m_new = bump ? m_blk : m_run;
                 const float alpha = bump ? ex2_approx(m_run - m_new) : 1.0f;
                 m_run = m_new;
                 const float m_sub = (m_run == kNegInf) ? 0.f : m_run;
+                const uint64_t nm2 = f2_pack(-m_sub, -m_sub);
 
-                uint32_t pk[C::BN / 2];
-                float sum0 = 0.f, sum1 = 0.f;
+                // P = exp2(s * scale * log2 e - m), rounded to 16 bits and written over S,
+                // 32 columns at a time.
+                uint64_t sum2 = f2_pack(0.f, 0.f);
 #pragma unroll
-                for (int i = 0; i < C::BN / 2; ++i) {
-                    const float p0 = ex2_approx(fmaf(s[2 * i], p.scale_log2, -m_sub));
-                    const float p1 = ex2_approx(fmaf(s[2 * i + 1], p.scale_log2, -m_sub));
-                    sum0 += p0;
-                    sum1 += p1;
-                    pk[i] = pack2<kBF16>(p0, p1);
+                for (int ch = 0; ch < kSC; ++ch) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const uint64_t a = fma2(f2_pack(__uint_as_float(u[ch][2 * i]),
+                                                        __uint_as_float(u[ch][2 * i + 1])),
+                                                c2, nm2);
+                        float a0, a1;
+                        f2_unpack(a, a0, a1);
+                        const float p0 = ex2_approx(a0);
+                        const float p1 = ex2_approx(a1);
+                        sum2 = add2(sum2, f2_pack(p0, p1));
+                        pk[i] = pack2<kBF16>(p0, p1);
+                    }
+                    tmem_st_32x32b_x16(tS + ch * 16, pk);
                 }
-                l_run = l_run * alpha + (sum0 + sum1);
+                l2 = fma2(l2, f2_pack(alpha, alpha), sum2);
 
-                if (j > 0) {
-                    // O of the previous block is complete before it may be rescaled and
-                    // before P of this block may be consumed.
+                if (kOPerIter && j > 0) {
+                    // NQ == 1: the next S is issued ahead of the previous P.V, so that P.V's
+                    // completion is awaited here before O may be rescaled.
                     ok = mbar_wait(bar(C::kBarODone + q), (it - 1) & 1u, wc);
                     if (!ok) break;
                     tc_fence_after();
-                    if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-#pragma unroll
-                        for (int ch = 0; ch < C::D / 32; ++ch) {
-                            uint32_t u[32];
-                            tmem_ld_32x32b_x32(tO + ch * 32, u);
-                            tmem_wait_ld(u);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-                            tmem_st_32x32b_x32(tO + ch * 32, u);
-                        }
-                    }
                 }
+                // NQ == 2: S of this block was issued after the previous P.V of this tile,
+                // so its completion (awaited above) implies that P.V has completed.
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll
-                for (int ch = 0; ch < C::BN / 64; ++ch) {
-                    uint32_t u[32];
+                    for (int ch = 0; ch < C::D / 32; ++ch) {
+                        uint32_t ov[32];
+                        tmem_ld_32x32b_x32(tO + ch * 32, ov);
+                        tmem_wait_ld(ov);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) u[i] = pk[ch * 32 + i];
-                    tmem_st_32x32b_x32(tS + ch * 32, u);
+                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st_32x32b_x32(tO + ch * 32, ov);
+                    }
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -418,20 +441,24 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             if (!ok) break;
 
             // ------------------------------------------------------------ epilogue ----
-            ok = mbar_wait(bar(C::kBarODone + q), (it - 1) & 1u, wc);
+            ok = mbar_wait(bar(C::kBarODone + q), kOPerIter ? ((it - 1) & 1u) : (tcount & 1u), wc);
             if (!ok) break;
             tc_fence_after();
+            ++tcount;
+            float l0, l1;
+            f2_unpack(l2, l0, l1);
+            const float l_run = l0 + l1;
             const float inv_l = (l_run > 0.f) ? 1.0f / l_run : 0.f;
 #pragma unroll
             for (int ch = 0; ch < C::D / 32; ++ch) {
-                uint32_t u[32];
-                tmem_ld_32x32b_x32(tO + ch * 32, u);
-                tmem_wait_ld(u);
+                uint32_t ov[32];
+                tmem_ld_32x32b_x32(tO + ch * 32, ov);
+                tmem_wait_ld(ov);
                 uint32_t w[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                    w[i] = pack2<kBF16>(__uint_as_float(u[2 * i]) * inv_l,
-                                        __uint_as_float(u[2 * i + 1]) * inv_l);
+                    w[i] = pack2<kBF16>(__uint_as_float(ov[2 * i]) * inv_l,
+                                        __uint_as_float(ov[2 * i + 1]) * inv_l);
                 if (row < p.Sq) {
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4)
