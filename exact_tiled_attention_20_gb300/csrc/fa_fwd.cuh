@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         for (int i = 0; i < C::kNumBars; ++i) {
             const bool by_warpgroup = (i >= C::kBarPFull && i < C::kBarPFull + C::NQ) ||
                                       (i >= C::kBarODrained && i < C::kBarODrained + C::NQ);
-            mbar_init(bar(i), by_warpgroup ? 128u : 1u);
+            mbar_init(bar(i), by_warpgroup ? 4u : 1u);  // one elected arrive per warp
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -435,7 +435,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(C::kBarPFull + q));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::kBarPFull + q));
                 ++it;
             }
             if (!ok) break;
@@ -467,7 +468,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(bar(C::kBarODrained + q));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::kBarODrained + q));
             if (p.lse && row < p.Sq) {
                 const float lse = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.69314718055994531f
                                                 : kNegInf;
