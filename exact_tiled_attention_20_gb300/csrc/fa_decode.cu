@@ -231,6 +231,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     __syncthreads();
     const uint32_t tmem = T.tmem_slot;
     const int total = T.total_items;
+    // The merge kernel may be scheduled now; it waits for this grid's results itself.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == kDecProducerWarp) {
         // -------------------------------------------------------------- producer ----
@@ -287,23 +289,30 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             constexpr uint32_t idesc_o = make_idesc_f16(128, 16, kBF16, true, false);
             uint32_t kv_it = 0, icount = 0, it_s = 0;
             bool ok = true;
+            const uint64_t dk0 = make_sdesc_sw128(sK, 16, 1024);
+            const uint64_t dq0 = make_sdesc_sw128(sQ, 16, 1024);
+            const uint64_t dv0 = make_sdesc_sw128(sV, kDecBN * 128, 1024);
+            const uint64_t dp0 = make_sdesc_sw128(sP, 16, 1024);
             auto issue_s = [&](uint32_t qs, uint32_t kst, uint32_t slot) {
+                const uint64_t a = dk0 + (uint64_t)((kst * kDecKVBytes) >> 4);
+                const uint64_t b = dq0 + (uint64_t)((qs * kDecQBytes) >> 4);
+                const uint32_t d = tmem + slot * 16;
+                umma_ss_imm<false>(d, a, b, idesc_s);
 #pragma unroll
-                for (int kk = 0; kk < kDecD / 16; ++kk) {
-                    const uint32_t a_addr = sK + kst * kDecKVBytes + (kk >> 2) * (kDecBN * 128) + (kk & 3) * 32;
-                    const uint32_t b_addr = sQ + qs * kDecQBytes + (kk >> 2) * 2048 + (kk & 3) * 32;
-                    umma_ss(tmem + slot * 16, make_sdesc_sw128(a_addr, 16, 1024),
-                            make_sdesc_sw128(b_addr, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 1; kk < kDecD / 16; ++kk)
+                    umma_ss_imm<true>(d, a + (uint64_t)(((kk >> 2) * (kDecBN * 128) + (kk & 3) * 32) >> 4),
+                                      b + (uint64_t)(((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), idesc_s);
             };
             auto issue_pv = [&](uint32_t vst, bool acc) {
+                const uint64_t a = dv0 + (uint64_t)((vst * kDecKVBytes) >> 4);
+                if (acc)
+                    umma_ss_imm<true>(tmem + 32, a, dp0, idesc_o);
+                else
+                    umma_ss_imm<false>(tmem + 32, a, dp0, idesc_o);
 #pragma unroll
-                for (int kk = 0; kk < kDecBN / 16; ++kk) {
-                    const uint32_t a_addr = sV + vst * kDecKVBytes + kk * (16 * 128);
-                    const uint32_t b_addr = sP + (kk >> 2) * 2048 + (kk & 3) * 32;
-                    umma_ss(tmem + 32, make_sdesc_sw128(a_addr, kDecBN * 128, 1024),
-                            make_sdesc_sw128(b_addr, 16, 1024), idesc_o, (acc || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 1; kk < kDecBN / 16; ++kk)
+                    umma_ss_imm<true>(tmem + 32, a + (uint64_t)((kk * (16 * 128)) >> 4),
+                                      dp0 + (uint64_t)(((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), idesc_o);
             };
             for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
                 const DecItem item = decode_item(T, p.B, p.Hkv, idx);
@@ -494,6 +503,9 @@ __global__ void __launch_bounds__(128)
     const float* orow = p.o_part + (size_t)bh * p.ns * kDecD;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float lse = kNegInf;
+    // The partials are written by the split kernel, which may still be running when this
+    // grid starts (programmatic dependent launch): wait for its completion here.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (n > 0) {
         float m = kNegInf;
         for (int c = lane; c < n; c += 32) m = fmaxf(m, lrow[c]);
@@ -503,7 +515,25 @@ __global__ void __launch_bounds__(128)
         for (int c = lane; c < n; c += 32) s += ex2_approx((lrow[c] - m) * kLog2e);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        for (int c = 0; c < n; ++c) {
+        // fixed summation order over the chunks; four loads in flight per lane
+        int c = 0;
+        for (; c + 4 <= n; c += 4) {
+            float4 v[4];
+            float w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                v[u] = *reinterpret_cast<const float4*>(orow + (size_t)(c + u) * kDecD + lane * 4);
+                w[u] = ex2_approx((lrow[c + u] - m) * kLog2e);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                acc[0] = fmaf(w[u], v[u].x, acc[0]);
+                acc[1] = fmaf(w[u], v[u].y, acc[1]);
+                acc[2] = fmaf(w[u], v[u].z, acc[2]);
+                acc[3] = fmaf(w[u], v[u].w, acc[3]);
+            }
+        }
+        for (; c < n; ++c) {
             const float w = ex2_approx((lrow[c] - m) * kLog2e);
             const float4 v = *reinterpret_cast<const float4*>(orow + (size_t)c * kDecD + lane * 4);
             acc[0] = fmaf(w, v.x, acc[0]);
@@ -568,11 +598,21 @@ fa_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
     else
         st = a.bf16 ? launch_split<16, true>(tq, tk, tv, p, grid, s) : launch_split<16, false>(tq, tk, tv, p, grid, s);
     if (st != FA_OK) return st;
-    const int cgrid = (a.B * a.Hq + 3) / 4;
-    if (a.bf16)
-        fa_decode_combine_kernel<true><<<cgrid, 128, 0, s>>>(p);
-    else
-        fa_decode_combine_kernel<false><<<cgrid, 128, 0, s>>>(p);
+    // The merge kernel is launched as a programmatic dependent of the split kernel: its
+    // launch overlaps the split kernel's tail, and it waits for the split results itself.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((a.B * a.Hq + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = a.bf16 ? cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<true>, p)
+                                 : cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<false>, p);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
