@@ -17,6 +17,8 @@ the pages as cited in that file's header:
   (page "flash attention-2 github", steps 1-2).
 * ``combine``  -- the log-sum-exp merge of partials (same snippet, step 3; the formula
   is the exact identity over a partition of the key set).
+* ``fwd(..., window=(left, right))`` -- sliding-window local attention (page
+  "flash-attention-v100", flash_attn_func window_size; "Changelog", "2.3").
 
 Parity pins: every function is pinned in ``tests/test_oracle.py`` against closed forms,
 the pages' worked mask examples, library routines and brute force (see that file).
@@ -59,7 +61,7 @@ def _load():
             path = os.environ.get("FA_ORACLE_LIB") or build()
             lib = ctypes.CDLL(path)
             L, D_, P, I = ctypes.c_long, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
-            lib.fa_oracle_fwd.argtypes = [P, P, P, I, L, L, L, L, L, L, D_, I, P, L, P, P, I]
+            lib.fa_oracle_fwd.argtypes = [P, P, P, I, L, L, L, L, L, L, D_, I, L, L, P, L, P, P, I]
             lib.fa_oracle_fwd.restype = I
             lib.fa_oracle_partial.argtypes = [P, P, P, I, L, L, L, L, L, L, L, L, L, D_, P, P]
             lib.fa_oracle_partial.restype = I
@@ -109,10 +111,13 @@ def _threads(n):
     return int(n) if n else (os.cpu_count() or 1)
 
 
-def fwd(q, k, v, scale: float, causal: bool = False, rows=None, nthreads=None):
+def fwd(q, k, v, scale: float, causal: bool = False, rows=None, nthreads=None,
+        window=(-1, -1)):
     """Exact attention forward, fp64.
 
-    q: [B, Sq, Hq, D], k/v: [B, Sk, Hkv, D] (same dtype).  Returns ``(o, lse)``:
+    q: [B, Sq, Hq, D], k/v: [B, Sk, Hkv, D] (same dtype).  ``window=(left, right)``
+    restricts query i to keys i+Sk-Sq-left .. i+Sk-Sq+right (-1: unbounded).
+    Returns ``(o, lse)``:
     with ``rows=None`` o is [B, Sq, Hq, D] and lse is [B, Hq, Sq]; with ``rows`` an
     (n, 3) integer array of (b, h, i) it returns o [n, D] and lse [n].
     """
@@ -134,9 +139,10 @@ def fwd(q, k, v, scale: float, causal: bool = False, rows=None, nthreads=None):
         o = np.zeros((r.shape[0], D), np.float64)
         lse = np.zeros((r.shape[0],), np.float64)
         rp, nr = _ptr(r), r.shape[0]
+    wl, wr = (int(window[0]), int(window[1]))
     rc = _load().fa_oracle_fwd(_ptr(qa), _ptr(ka), _ptr(va), dt, B, Sq, Sk, Hq, Hkv, D,
-                               float(scale), int(bool(causal)), rp, nr, _ptr(o), _ptr(lse),
-                               _threads(nthreads))
+                               float(scale), int(bool(causal)), wl, wr, rp, nr, _ptr(o),
+                               _ptr(lse), _threads(nthreads))
     if rc:
         raise ValueError(f"fa_oracle_fwd failed with code {rc}")
     return o, lse

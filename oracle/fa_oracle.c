@@ -21,6 +21,12 @@
  *    and chunk (the log of the sum of exponentials), and a separate step merges them.
  *    The merge is the log-sum-exp identity over a partition of the key set, written
  *    out in fa_oracle_combine below.
+ *  - same page, "How to use FlashAttention" (flash_attn_func, window_size) and
+ *    "Changelog", "2.3: Local (i.e., sliding window) attention": with a window
+ *    (left, right), query i attends only to keys j with
+ *    i + Sk - Sq - left <= j <= i + Sk - Sq + right; -1 means unbounded on that side.
+ *    With the causal flag the right bound is at most i + Sk - Sq (the plainest reading
+ *    of combining the two: both masks apply).
  *
  * Readings where the pages are silent: the per-row log-sum-exp is the natural log of
  * the sum of exp over the *scaled, masked* scores; a row with no visible key has
@@ -118,6 +124,7 @@ typedef struct {
     long B, Sq, Sk, Hq, Hkv, D;
     double scale;
     int causal;
+    long win_left, win_right; /* sliding window, -1 = unbounded */
     const int64_t *rows; /* (b, h, i) triples, or NULL for every row */
     const int32_t *kv_lens; /* decode mode: per-sequence key counts, else NULL */
     long n_items;
@@ -165,12 +172,20 @@ static void fwd_one(const fwd_job *J, long item, double *s_buf) {
     size_t q_off = (((size_t)b * J->Sq + i) * J->Hq + h) * J->D;
     size_t kv_off = (((size_t)b * J->Sk) * J->Hkv + hk) * J->D;
     size_t kv_stride = (size_t)J->Hkv * J->D;
-    long j1 = J->Sk;
+    long j0 = 0, j1 = J->Sk;
     if (J->causal) {
         long lim = i + J->Sk - J->Sq + 1; /* bottom-right aligned: j <= i + Sk - Sq */
         if (lim < j1) j1 = lim;
     }
-    attend_row(J->q, J->k, J->v, J->dtype, q_off, kv_off, kv_stride, (int)J->D, 0, j1, J->scale,
+    if (J->win_right >= 0) {
+        long lim = i + J->Sk - J->Sq + J->win_right + 1;
+        if (lim < j1) j1 = lim;
+    }
+    if (J->win_left >= 0) {
+        long lim = i + J->Sk - J->Sq - J->win_left;
+        if (lim > j0) j0 = lim;
+    }
+    attend_row(J->q, J->k, J->v, J->dtype, q_off, kv_off, kv_stride, (int)J->D, j0, j1, J->scale,
                s_buf, o, lse);
 }
 
@@ -229,14 +244,16 @@ static int run_pool(fwd_job *J) {
 
 /*
  * Exact attention forward for [B, S, H, D] tensors (page "flash-attention-v100",
- * "How to use FlashAttention", flash_attn_func).
+ * "How to use FlashAttention", flash_attn_func), optionally restricted to a sliding
+ * window (win_left / win_right, -1 = unbounded).
  *   rows == NULL: every row; o is [B, Sq, Hq, D], lse is [B, Hq, Sq].
  *   rows != NULL: n_rows (b, h, i) triples; o is [n_rows, D], lse is [n_rows].
  * Returns 0 on success, 2 on a bad argument, 3 when out of host memory.
  */
 int fa_oracle_fwd(const void *q, const void *k, const void *v, int dtype, long B, long Sq,
-                  long Sk, long Hq, long Hkv, long D, double scale, int causal,
-                  const int64_t *rows, long n_rows, double *o, double *lse, int nthreads) {
+                  long Sk, long Hq, long Hkv, long D, double scale, int causal, long win_left,
+                  long win_right, const int64_t *rows, long n_rows, double *o, double *lse,
+                  int nthreads) {
     if (!q || !k || !v || !o || !lse) return 2;
     if (B < 0 || Sq < 0 || Sk < 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return 2;
     if (Hq % Hkv != 0) return 2;
@@ -255,6 +272,8 @@ int fa_oracle_fwd(const void *q, const void *k, const void *v, int dtype, long B
     J.D = D;
     J.scale = scale;
     J.causal = causal;
+    J.win_left = win_left;
+    J.win_right = win_right;
     J.o = o;
     J.lse = lse;
     J.nthreads = nthreads;

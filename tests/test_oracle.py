@@ -292,3 +292,65 @@ def test_bad_arguments_are_rejected():
     q, kc, vc, _ = _decode_case()
     with pytest.raises(ValueError):
         oracle.decode(q, kc, vc, np.array([41, 1, 1], np.int32), scale=1.0)  # > Smax
+
+
+# ---------------------------------------------------------- sliding window ----
+
+def _band_keep(Sq, Sk, left, right, causal):
+    """Visible-key mask of a sliding window from numpy's triu/tril (bottom-right aligned)."""
+    keep = np.ones((Sq, Sk), bool)
+    off = Sk - Sq
+    if right >= 0:
+        keep &= np.tril(np.ones((Sq, Sk), bool), k=off + right)
+    if causal:
+        keep &= np.tril(np.ones((Sq, Sk), bool), k=off)
+    if left >= 0:
+        keep &= np.triu(np.ones((Sq, Sk), bool), k=off - left)
+    return keep
+
+
+@pytest.mark.parametrize("sq,sk,left,right,causal", [
+    (9, 9, 2, 1, False), (9, 9, 3, -1, True), (5, 12, 0, 0, False), (12, 5, 1, 2, False),
+    (12, 5, 4, 0, True), (7, 7, -1, 2, False), (6, 20, 3, 3, True)])
+def test_window_matches_band_mask(sq, sk, left, right, causal):
+    """Q = 0 gives the mean over exactly the visible keys: the band mask is recovered."""
+    D = max(sk, 4)
+    q = np.zeros((1, sq, 1, D))
+    k = _rand(1, sk, 1, D)
+    v = np.zeros((1, sk, 1, D))
+    for j in range(sk):
+        v[0, j, 0, j] = 1.0
+    o, lse = oracle.fwd(q, k, v, scale=0.5, causal=causal, window=(left, right))
+    keep = _band_keep(sq, sk, left, right, causal)
+    assert np.array_equal(o[0, :, 0, :sk] > 0, keep)
+    for i in range(sq):
+        n = keep[i].sum()
+        if n == 0:
+            assert lse[0, 0, i] == -np.inf and np.all(o[0, i] == 0)
+        else:
+            assert lse[0, 0, i] == pytest.approx(math.log(n), abs=1e-14)
+
+
+def test_window_special_cases_reduce_to_full_and_causal():
+    q, k, v = _rand(2, 11, 2, 8), _rand(2, 11, 1, 8), _rand(2, 11, 1, 8)
+    full = oracle.fwd(q, k, v, scale=0.6)
+    causal = oracle.fwd(q, k, v, scale=0.6, causal=True)
+    for a, b in ((oracle.fwd(q, k, v, scale=0.6, window=(-1, -1)), full),
+                 (oracle.fwd(q, k, v, scale=0.6, window=(100, 100)), full),
+                 (oracle.fwd(q, k, v, scale=0.6, window=(-1, 0)), causal),
+                 (oracle.fwd(q, k, v, scale=0.6, causal=True, window=(100, 5)), causal)):
+        assert np.allclose(a[0], b[0], atol=1e-14) and np.allclose(a[1], b[1], atol=1e-14)
+
+
+def test_window_matches_scipy_with_band_mask():
+    B, Sq, Sk, Hq, Hkv, D = 1, 10, 13, 2, 1, 8
+    q, k, v = _rand(B, Sq, Hq, D), _rand(B, Sk, Hkv, D), _rand(B, Sk, Hkv, D)
+    left, right = 3, 2
+    o, lse = oracle.fwd(q, k, v, scale=0.4, window=(left, right))
+    keep = _band_keep(Sq, Sk, left, right, False)
+    for h in range(Hq):
+        s = 0.4 * q[0, :, h] @ k[0, :, 0].T
+        for i in range(Sq):
+            p = scipy.special.softmax(s[i][keep[i]])
+            assert np.allclose(o[0, i, h], p @ v[0, keep[i], 0], atol=1e-12)
+            assert lse[0, h, i] == pytest.approx(scipy.special.logsumexp(s[i][keep[i]]), abs=1e-12)

@@ -16,7 +16,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "fa_oracle.c")
 
 MUTATIONS = {
-    "top_left_causal": ("long lim = i + J->Sk - J->Sq + 1;", "long lim = i + 1;"),
+    "top_left_causal": ("long lim = i + J->Sk - J->Sq + 1; /* bottom-right", "long lim = i + 1; /* bottom-right"),
+    "window_left_off_by_one": ("long lim = i + J->Sk - J->Sq - J->win_left;",
+                               "long lim = i + J->Sk - J->Sq - J->win_left + 1;"),
     "gqa_modulo": ("long hk = h / g; /* grouped-query head map */", "long hk = h % J->Hkv;"),
     "dropped_scale": ("s_buf[t] = scale * dot;", "s_buf[t] = dot;"),
     "lse_without_max": ("*lse = m + log(l);", "*lse = log(l);"),
