@@ -17,6 +17,8 @@ the pages as cited in that file's header:
   (page "flash attention-2 github", steps 1-2).
 * ``combine``  -- the log-sum-exp merge of partials (same snippet, step 3; the formula
   is the exact identity over a partition of the key set).
+* ``decode_paged`` -- decode over a paged KV cache addressed through a block table
+  (flash_attn_with_kvcache block_table; "Changelog", "2.5: Paged KV cache").
 * ``fwd(..., window=(left, right))`` -- sliding-window local attention (page
   "flash-attention-v100", flash_attn_func window_size; "Changelog", "2.3").
 
@@ -69,6 +71,9 @@ def _load():
             lib.fa_oracle_decode.restype = I
             lib.fa_oracle_combine.argtypes = [P, P, L, L, P, P]
             lib.fa_oracle_combine.restype = I
+            lib.fa_oracle_decode_paged.argtypes = [P, P, P, I, P, P, L, L, L, L, L, L, L, D_, P,
+                                                   P, I]
+            lib.fa_oracle_decode_paged.restype = I
             _lib = lib
     return _lib
 
@@ -200,3 +205,25 @@ def combine(o_parts, lse_parts):
     if rc:
         raise ValueError(f"fa_oracle_combine failed with code {rc}")
     return o, float(lse[0])
+
+
+def decode_paged(q, k_pages, v_pages, block_table, kv_lens, scale: float, nthreads=None):
+    """Decode over a paged cache: k_pages/v_pages [num_pages, page_size, Hkv, D];
+    block_table [B, max_pages] ints; kv_lens [B].  Returns o [B, Hq, D], lse [B, Hq]."""
+    qa, dt = _as_input(q)
+    ka, _ = _as_input(k_pages)
+    va, _ = _as_input(v_pages)
+    if qa.ndim == 4:
+        qa = qa.reshape(qa.shape[0], qa.shape[2], qa.shape[3])
+    B, Hq, D = qa.shape
+    num_pages, page_size, Hkv, _ = ka.shape
+    bt = np.ascontiguousarray(np.asarray(block_table, dtype=np.int32))
+    lens = np.ascontiguousarray(np.asarray(kv_lens, dtype=np.int32).reshape(-1))
+    o = np.zeros((B, Hq, D), np.float64)
+    lse = np.zeros((B, Hq), np.float64)
+    rc = _load().fa_oracle_decode_paged(_ptr(qa), _ptr(ka), _ptr(va), dt, _ptr(bt), _ptr(lens), B,
+                                        Hq, Hkv, D, num_pages, page_size, bt.shape[1],
+                                        float(scale), _ptr(o), _ptr(lse), _threads(nthreads))
+    if rc:
+        raise ValueError(f"fa_oracle_decode_paged failed with code {rc}")
+    return o, lse

@@ -21,6 +21,10 @@
  *    and chunk (the log of the sum of exponentials), and a separate step merges them.
  *    The merge is the log-sum-exp identity over a partition of the key set, written
  *    out in fa_oracle_combine below.
+ *  - same page, "How to use FlashAttention" (flash_attn_with_kvcache, block_table) and
+ *    "Changelog", "2.5: Paged KV cache": with a block table, key j of sequence b lives
+ *    in page block_table[b][j / page_size] at row j % page_size of a
+ *    [num_pages, page_size, Hkv, D] cache.
  *  - same page, "How to use FlashAttention" (flash_attn_func, window_size) and
  *    "Changelog", "2.3: Local (i.e., sliding window) attention": with a window
  *    (left, right), query i attends only to keys j with
@@ -378,4 +382,57 @@ int fa_oracle_combine(const double *o_parts, const double *lse_parts, long n, lo
     }
     *lse = total;
     return 0;
+}
+
+/*
+ * Single-token decode over a paged KV cache (page "flash-attention-v100",
+ * flash_attn_with_kvcache with block_table; "Changelog", "2.5: Paged KV cache"):
+ * k_pages / v_pages are [num_pages, page_size, Hkv, D]; block_table is
+ * [B, max_pages] (host int32); key j of sequence b is row j % page_size of page
+ * block_table[b][j / page_size].  The keys of each sequence are first gathered into a
+ * contiguous fp64 buffer in that order, then the decode definition is applied.
+ */
+int fa_oracle_decode_paged(const void *q, const void *k_pages, const void *v_pages, int dtype,
+                           const int32_t *block_table, const int32_t *kv_lens, long B, long Hq,
+                           long Hkv, long D, long num_pages, long page_size, long max_pages,
+                           double scale, double *o, double *lse, int nthreads) {
+    if (!q || !k_pages || !v_pages || !block_table || !kv_lens || !o || !lse) return 2;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || page_size <= 0 || max_pages <= 0) return 2;
+    if (Hq % Hkv != 0) return 2;
+    const long smax = page_size * max_pages;
+    for (long b = 0; b < B; ++b) {
+        if (kv_lens[b] < 0 || kv_lens[b] > smax) return 2;
+        for (long t = 0; t * page_size < kv_lens[b]; ++t) {
+            const long pg = block_table[b * max_pages + t];
+            if (pg < 0 || pg >= num_pages) return 2;
+        }
+    }
+    const size_t row = (size_t)Hkv * D;
+    double *kc = (double *)malloc(sizeof(double) * (size_t)B * smax * row);
+    double *vc = (double *)malloc(sizeof(double) * (size_t)B * smax * row);
+    double *qd = (double *)malloc(sizeof(double) * (size_t)B * Hq * D);
+    if (!kc || !vc || !qd) {
+        free(kc);
+        free(vc);
+        free(qd);
+        return 3;
+    }
+    for (size_t n = 0; n < (size_t)B * Hq * D; ++n) qd[n] = load_elem(q, dtype, n);
+    for (long b = 0; b < B; ++b) {
+        for (long j = 0; j < kv_lens[b]; ++j) {
+            const long pg = block_table[b * max_pages + j / page_size];
+            const size_t src = ((size_t)pg * page_size + (size_t)(j % page_size)) * row;
+            const size_t dst = ((size_t)b * smax + (size_t)j) * row;
+            for (size_t e = 0; e < row; ++e) {
+                kc[dst + e] = load_elem(k_pages, dtype, src + e);
+                vc[dst + e] = load_elem(v_pages, dtype, src + e);
+            }
+        }
+    }
+    int rc = fa_oracle_decode(qd, kc, vc, ORC_F64, kv_lens, B, Hq, Hkv, D, smax, scale, o, lse,
+                              nthreads);
+    free(kc);
+    free(vc);
+    free(qd);
+    return rc;
 }

@@ -354,3 +354,61 @@ def test_window_matches_scipy_with_band_mask():
             p = scipy.special.softmax(s[i][keep[i]])
             assert np.allclose(o[0, i, h], p @ v[0, keep[i], 0], atol=1e-12)
             assert lse[0, h, i] == pytest.approx(scipy.special.logsumexp(s[i][keep[i]]), abs=1e-12)
+
+
+# ---------------------------------------------------------------- paged cache ----
+
+def _paged_case(B=3, Hq=4, Hkv=2, D=8, page=4, max_pages=5, seed=11):
+    rng = np.random.default_rng(seed)
+    smax = page * max_pages
+    q = rng.standard_normal((B, 1, Hq, D))
+    kc = rng.standard_normal((B, smax, Hkv, D))
+    vc = rng.standard_normal((B, smax, Hkv, D))
+    lens = np.array([smax, 7, 0][:B], np.int32)
+    return q, kc, vc, lens
+
+
+def test_paged_identity_table_equals_contiguous_decode():
+    q, kc, vc, lens = _paged_case()
+    B, smax, Hkv, D = kc.shape
+    page, max_pages = 4, 5
+    k_pages = kc.reshape(B * max_pages, page, Hkv, D)
+    v_pages = vc.reshape(B * max_pages, page, Hkv, D)
+    table = np.arange(B * max_pages, dtype=np.int32).reshape(B, max_pages)
+    o1, l1 = oracle.decode_paged(q, k_pages, v_pages, table, lens, scale=0.4)
+    o2, l2 = oracle.decode(q, kc, vc, lens, scale=0.4)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_paged_permuted_pages_equal_contiguous_decode():
+    """Pages scattered through the pool by a random permutation (and spare pages that
+    no sequence uses) give the same result as the contiguous cache."""
+    q, kc, vc, lens = _paged_case()
+    B, smax, Hkv, D = kc.shape
+    page, max_pages = 4, 5
+    n_pool = B * max_pages + 3
+    perm = RNG.permutation(n_pool)[: B * max_pages]
+    k_pages = RNG.standard_normal((n_pool, page, Hkv, D))
+    v_pages = RNG.standard_normal((n_pool, page, Hkv, D))
+    table = np.zeros((B, max_pages), np.int32)
+    for b in range(B):
+        for t in range(max_pages):
+            pg = perm[b * max_pages + t]
+            table[b, t] = pg
+            k_pages[pg] = kc[b, t * page:(t + 1) * page]
+            v_pages[pg] = vc[b, t * page:(t + 1) * page]
+    o1, l1 = oracle.decode_paged(q, k_pages, v_pages, table, lens, scale=0.4)
+    o2, l2 = oracle.decode(q, kc, vc, lens, scale=0.4)
+    assert np.allclose(o1, o2, atol=1e-15) and np.array_equal(np.isfinite(l1), np.isfinite(l2))
+    fin = np.isfinite(l2)
+    assert np.allclose(l1[fin], l2[fin], atol=1e-15)
+
+
+def test_paged_rejects_out_of_pool_pages():
+    q, kc, vc, lens = _paged_case()
+    B, smax, Hkv, D = kc.shape
+    k_pages = kc.reshape(B * 5, 4, Hkv, D)
+    table = np.arange(B * 5, dtype=np.int32).reshape(B, 5)
+    table[0, 1] = 99
+    with pytest.raises(ValueError):
+        oracle.decode_paged(q, k_pages, k_pages, table, lens, scale=0.4)

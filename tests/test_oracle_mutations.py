@@ -26,6 +26,8 @@ MUTATIONS = {
                               "double w = exp(total - lse_parts[s]);"),
     "v_read_from_k": ("o[d] += p * load_elem(v, dtype, vbase + d);",
                       "o[d] += p * load_elem(k, dtype, vbase + d);"),
+    "paged_table_stride": ("const long pg = block_table[b * max_pages + j / page_size];",
+                           "const long pg = block_table[b + j / page_size];"),
     "bf16_decode_shift": ("uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h << 15;"),
 }
 
