@@ -50,6 +50,8 @@ def load():
         P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, I, P]
         lib.fa_fwd.restype = I
+        lib.fa_fwd_window.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, I, P]
+        lib.fa_fwd_window.restype = I
         lib.fa_decode_workspace_bytes.argtypes = [I, I, I, I]
         lib.fa_decode_workspace_bytes.restype = SZ
         lib.fa_decode_default_splits.argtypes = [I, I, I, I]
@@ -88,8 +90,9 @@ def fa_last_device_status() -> int:
 
 
 def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-           return_lse: bool = True, stream=None):
-    """Exact attention forward through fa_fwd.  q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D].
+           return_lse: bool = True, stream=None, window=None):
+    """Exact attention forward through fa_fwd (or fa_fwd_window when ``window=(left,
+    right)`` is given; -1 = unbounded side).  q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D].
 
     Returns (o, lse): o like q, lse fp32 [B, Hq, Sq] (None if return_lse is False and no
     lse buffer was given).  scale defaults to 1/sqrt(D).
@@ -115,11 +118,17 @@ def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, 
             raise ValueError("lse must be [B, Hq, Sq]")
     sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
     with torch.cuda.device(q.device):
-        st = load().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                           lse.data_ptr() if lse is not None else None, B, Sq, Sk, Hq, Hkv, D, sc,
-                           int(bool(causal)), _DTYPE[q.dtype], _stream_handle(stream))
+        lp = lse.data_ptr() if lse is not None else None
+        if window is None:
+            st = load().fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lp, B, Sq,
+                               Sk, Hq, Hkv, D, sc, int(bool(causal)), _DTYPE[q.dtype],
+                               _stream_handle(stream))
+        else:
+            st = load().fa_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lp,
+                                      B, Sq, Sk, Hq, Hkv, D, sc, int(bool(causal)), int(window[0]),
+                                      int(window[1]), _DTYPE[q.dtype], _stream_handle(stream))
     if st != FA_OK:
-        raise FaError(st, "fa_fwd")
+        raise FaError(st, "fa_fwd_window" if window is not None else "fa_fwd")
     return out, lse
 
 
@@ -218,4 +227,55 @@ def fa_decode_splitkv_noalloc(q, k_cache, v_cache, kv_lens, scale: float | None 
                                            _stream_handle(stream))
     if st != FA_OK:
         raise FaError(st, "fa_decode_splitkv_noalloc")
+    return out, lse
+
+
+_paged_declared = False
+
+
+def fa_decode_splitkv_paged(q, k_pages, v_pages, block_table, kv_lens, scale: float | None = None,
+                            num_splits: int = 0, workspace=None, out=None, lse=None, stream=None):
+    """Split-KV decode over a paged cache through fa_decode_splitkv_paged.
+
+    q [B,1,Hq,D]; k_pages/v_pages [num_pages, page_size, Hkv, D]; block_table int32
+    [B, max_pages_per_seq] and kv_lens int32 [B] on the device.  Returns (o, lse)."""
+    global _paged_declared
+    lib = load()
+    if not _paged_declared:
+        P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.fa_decode_splitkv_paged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P,
+                                                SZ, I, P]
+        lib.fa_decode_splitkv_paged.restype = I
+        _paged_declared = True
+    if q.dtype not in _DTYPE:
+        raise TypeError("q/k_pages/v_pages must be bf16 or fp16")
+    for name, t in (("q", q), ("k_pages", k_pages), ("v_pages", v_pages)):
+        _check_cuda(name, t, q.dtype)
+    _check_cuda("block_table", block_table, torch.int32)
+    _check_cuda("kv_lens", kv_lens, torch.int32)
+    B, _, Hq, D = q.shape
+    num_pages, page_size, Hkv, _ = k_pages.shape
+    max_pages = block_table.shape[1]
+    with torch.cuda.device(q.device):
+        ns = int(num_splits) if num_splits and num_splits > 0 else \
+            lib.fa_decode_default_splits(B, Hkv, page_size * max_pages, 0)
+        if ns <= 0:
+            raise FaError(FA_ERR_CUDA, "fa_decode_default_splits")
+        ns = min(ns, page_size * max_pages)
+        if workspace is None:
+            workspace = torch.empty(lib.fa_decode_workspace_bytes(B, Hq, D, ns), dtype=torch.uint8,
+                                    device=q.device)
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+        sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+        st = lib.fa_decode_splitkv_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                                         block_table.data_ptr(), kv_lens.data_ptr(), out.data_ptr(),
+                                         lse.data_ptr(), B, Hq, Hkv, D, num_pages, page_size,
+                                         max_pages, sc, ns, workspace.data_ptr(),
+                                         workspace.numel() * workspace.element_size(),
+                                         _DTYPE[q.dtype], _stream_handle(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_decode_splitkv_paged")
     return out, lse

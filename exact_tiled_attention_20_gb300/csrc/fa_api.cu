@@ -110,14 +110,15 @@ using namespace fa;
 
 extern "C" {
 
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq,
-                 int Sk, int Hq, int Hkv, int D, float scale, int causal, fa_dtype dtype,
-                 fa_stream_t stream) {
+fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int Sq, int Sk, int Hq, int Hkv, int D, float scale, int causal,
+                        int window_left, int window_right, fa_dtype dtype, fa_stream_t stream) {
     if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
     if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_INVALID_ARG;
     if (B <= 0 || Sq <= 0 || Sk <= 0 || Hq <= 0 || Hkv <= 0) return FA_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+    if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
     if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_UNSUPPORTED;
     if (D != 64 && D != 96 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
@@ -126,8 +127,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
         return FA_ERR_UNSUPPORTED;
     DeviceInfo di;
     if (!device_info(&di)) return FA_ERR_CUDA;
-    FwdArgs a{q, k, v, o, lse, B, Sq, Sk, Hq, Hkv, D, scale, causal, dtype == FA_BF16,
-              di.num_sms, di.status};
+    FwdArgs a{q, k, v, o, lse, B, Sq, Sk, Hq, Hkv, D, scale, causal, window_left, window_right,
+              dtype == FA_BF16, di.num_sms, di.status};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (D) {
         case 64: return launch_fwd_d64(a, s);
@@ -135,6 +136,13 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
         case 128: return launch_fwd_d128(a, s);
         default: return launch_fwd_d256(a, s);
     }
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Sq,
+                 int Sk, int Hq, int Hkv, int D, float scale, int causal, fa_dtype dtype,
+                 fa_stream_t stream) {
+    return fa_fwd_window(q, k, v, o, lse, B, Sq, Sk, Hq, Hkv, D, scale, causal, -1, -1, dtype,
+                         stream);
 }
 
 size_t fa_decode_workspace_bytes(int B, int Hq, int D, int num_splits) {
@@ -163,10 +171,14 @@ int fa_decode_default_splits(int B, int Hkv, int max_kv_len, int num_sms) {
     return (int)ns;
 }
 
-fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
-                            const int32_t* kv_lens, void* o, float* lse, int B, int Hq, int Hkv,
-                            int D, int Smax, float scale, int num_splits, void* workspace,
-                            size_t workspace_bytes, fa_dtype dtype, fa_stream_t stream) {
+namespace {
+
+// Shared validation and dispatch of the contiguous and paged decode entry points.
+fa_status decode_common(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_table, const int32_t* kv_lens, void* o, float* lse,
+                        int B, int Hq, int Hkv, int D, int Smax, int num_pages, int page_size,
+                        int max_pages, float scale, int num_splits, void* workspace,
+                        size_t workspace_bytes, fa_dtype dtype, fa_stream_t stream) {
     if (!q || !k_cache || !v_cache || !kv_lens || !o) return FA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
         (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
@@ -176,8 +188,8 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
     if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
     if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_UNSUPPORTED;
-    if (D != 128 && D != 64) return FA_ERR_UNSUPPORTED;
-    if (Hq / Hkv > 16) return FA_ERR_UNSUPPORTED;
+    if (D != 128) return FA_ERR_UNSUPPORTED;
+    if (Hq / Hkv > 16 || B > 1024) return FA_ERR_UNSUPPORTED;
     if ((long long)B * Smax > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
     DeviceInfo di;
     if (!device_info(&di)) return FA_ERR_CUDA;
@@ -190,8 +202,35 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
     float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                                ((rows * D * sizeof(float) + 255) & ~size_t(255)));
     DecodeArgs a{q, k_cache, v_cache, kv_lens, o, lse, B, Hq, Hkv, D, Smax, scale, num_splits,
-                 o_part, lse_part, dtype == FA_BF16, di.num_sms, di.status};
+                 o_part, lse_part, block_table, num_pages, page_size, max_pages,
+                 dtype == FA_BF16, di.num_sms, di.status};
     return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* kv_lens, void* o, float* lse, int B, int Hq, int Hkv,
+                            int D, int Smax, float scale, int num_splits, void* workspace,
+                            size_t workspace_bytes, fa_dtype dtype, fa_stream_t stream) {
+    return decode_common(q, k_cache, v_cache, nullptr, kv_lens, o, lse, B, Hq, Hkv, D, Smax, 0, 0,
+                         0, scale, num_splits, workspace, workspace_bytes, dtype, stream);
+}
+
+fa_status fa_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_pages,
+                                  const int32_t* block_table, const int32_t* kv_lens, void* o,
+                                  float* lse, int B, int Hq, int Hkv, int D, int num_pages,
+                                  int page_size, int max_pages_per_seq, float scale,
+                                  int num_splits, void* workspace, size_t workspace_bytes,
+                                  fa_dtype dtype, fa_stream_t stream) {
+    if (!block_table || (reinterpret_cast<uintptr_t>(block_table) & 3u)) return FA_ERR_INVALID_ARG;
+    if (num_pages <= 0 || max_pages_per_seq <= 0 || page_size <= 0) return FA_ERR_INVALID_ARG;
+    if (page_size % 128 != 0) return FA_ERR_UNSUPPORTED;
+    const long long smax = (long long)page_size * max_pages_per_seq;
+    if (smax > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    return decode_common(q, k_pages, v_pages, block_table, kv_lens, o, lse, B, Hq, Hkv, D,
+                         (int)smax, num_pages, page_size, max_pages_per_seq, scale, num_splits,
+                         workspace, workspace_bytes, dtype, stream);
 }
 
 const char* fa_status_string(fa_status s) {

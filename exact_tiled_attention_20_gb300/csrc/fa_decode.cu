@@ -42,6 +42,11 @@ struct DecParams {
     void* o;          // [B, Hq, D]
     float* lse;       // [B, Hq] or null
     int q_rows;  // query-head rows per Q box (min(16, Hq)); rows past it are never read
+    // Paged cache (page "flash-attention-v100", flash_attn_with_kvcache block_table;
+    // "Changelog", "2.5: Paged KV cache"): key r of sequence b is row r % page_size of
+    // page block_table[b * max_pages + r / page_size]; page_size is a multiple of 128.
+    const int32_t* block_table;  // null: contiguous [B, Smax, Hkv, D] cache
+    int page_size, max_pages;
     int* status;
 };
 
@@ -248,16 +253,27 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 for (int a = 0; a < kDecDA; ++a)
                     tma_load_4d(sQ + qs * kDecQBytes + a * 2048, &tm_q, bar(kDBarQFull + qs), a * 64,
                                 it.hk * p.group, 0, it.b);
+                // Paged caches: the page of the next tile is fetched while this one waits.
+                auto page_of = [&](int r) -> int {
+                    return p.block_table[(size_t)it.b * p.max_pages + r / p.page_size];
+                };
+                int next_page = (p.block_table && it.ntiles > 0) ? page_of(it.k0) : 0;
                 for (int j = 0; j < it.ntiles && ok; ++j) {
                     const uint32_t st = kv_it % kDecNS;
                     const uint32_t ph = ((kv_it / kDecNS) & 1u) ^ 1u;
                     const int row = it.k0 + j * kDecBN;
+                    int c2 = row, c3 = it.b;  // contiguous: (key row, sequence)
+                    if (p.block_table) {      // paged: (row within page, page)
+                        c2 = row % p.page_size;
+                        c3 = next_page;
+                        if (j + 1 < it.ntiles) next_page = page_of(row + kDecBN);
+                    }
                     ok = mbar_wait(bar(kDBarKEmpty + st), ph, wc);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(kDBarKFull + st), kDecKVBytes);
                     for (int a = 0; a < kDecDA; ++a)
                         tma_load_4d(sK + st * kDecKVBytes + a * (kDecBN * 128), &tm_k,
-                                    bar(kDBarKFull + st), a * 64, it.hk, row, it.b);
+                                    bar(kDBarKFull + st), a * 64, it.hk, c2, c3);
                     ok = mbar_wait(bar(kDBarVEmpty + st), ph, wc);
                     if (!ok) {
                         mbar_wait_drain(bar(kDBarKFull + st), (kv_it / kDecNS) & 1u);
@@ -266,7 +282,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     mbar_arrive_expect_tx(bar(kDBarVFull + st), kDecKVBytes);
                     for (int a = 0; a < kDecDA; ++a)
                         tma_load_4d(sV + st * kDecKVBytes + a * (kDecBN * 128), &tm_v,
-                                    bar(kDBarVFull + st), a * 64, it.hk, row, it.b);
+                                    bar(kDBarVFull + st), a * 64, it.hk, c2, c3);
                     ++kv_it;
                 }
                 ++icount;
@@ -569,9 +585,12 @@ fa_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
     const int g = a.Hq / a.Hkv;
     CUtensorMap tq, tk, tv;
     const int q_rows = a.Hq < 16 ? a.Hq : 16;
+    // Contiguous caches are [B, Smax, Hkv, D]; paged pools are [num_pages, page_size, Hkv, D].
+    const uint64_t rows_dim = a.block_table ? (uint64_t)a.page_size : (uint64_t)a.Smax;
+    const uint64_t outer_dim = a.block_table ? (uint64_t)a.num_pages : (uint64_t)a.B;
     if (!encode_tmap_4d_box(&tq, a.q, a.bf16, a.D, a.Hq, 1, a.B, q_rows, 1) ||
-        !encode_tmap_4d(&tk, a.k_cache, a.bf16, a.D, a.Hkv, a.Smax, a.B, kDecBN) ||
-        !encode_tmap_4d(&tv, a.v_cache, a.bf16, a.D, a.Hkv, a.Smax, a.B, kDecBN))
+        !encode_tmap_4d(&tk, a.k_cache, a.bf16, a.D, a.Hkv, rows_dim, outer_dim, kDecBN) ||
+        !encode_tmap_4d(&tv, a.v_cache, a.bf16, a.D, a.Hkv, rows_dim, outer_dim, kDecBN))
         return FA_ERR_CUDA;
     DecParams p;
     p.B = a.B;
@@ -588,6 +607,9 @@ fa_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
     p.lse = a.lse;
     p.status = a.dev_status;
     p.q_rows = q_rows;
+    p.block_table = a.block_table;
+    p.page_size = a.page_size;
+    p.max_pages = a.max_pages;
     const long long items_max = (long long)a.B * a.Hkv * a.num_splits;
     const int grid = (int)(items_max < a.num_sms ? items_max : a.num_sms);
     fa_status st;

@@ -37,6 +37,10 @@ namespace fa {
 struct FwdParams {
     int B, Sq, Sk, Hq, Hkv, group;
     int causal;
+    // Sliding window (page "flash-attention-v100", flash_attn_func window_size): query i
+    // sees keys in [i + Sk - Sq - win_left, i + Sk - Sq + hi_off]; has_lo / has_hi say
+    // whether each bound applies (hi_off = 0 under the causal flag).
+    int has_lo, win_left, has_hi, hi_off;
     float scale_log2;  // softmax scale * log2(e)
     int num_qb;        // query blocks of NQ * 128 rows per (b, h)
     int num_tiles;     // B * Hq * num_qb
@@ -85,7 +89,7 @@ struct FwdConfig {
 };
 
 struct TileCoord {
-    int b, h, hk, m0, n_kv;
+    int b, h, hk, m0, j0, n_kv;  // K/V blocks j0 .. j0 + n_kv - 1
 };
 
 template <class C>
@@ -99,12 +103,18 @@ __device__ __forceinline__ TileCoord decode_tile(const FwdParams& p, int t) {
     c.b = bh / p.Hq;
     c.hk = c.h / p.group;
     c.m0 = qb * (C::NQ * C::BM);
-    int kv_end = p.Sk;
-    if (p.causal) {
-        const int last_row = min(p.Sq, c.m0 + C::NQ * C::BM) - 1;
-        kv_end = min(kv_end, last_row + (p.Sk - p.Sq) + 1);
+    const int off = p.Sk - p.Sq;
+    const int last_row = min(p.Sq, c.m0 + C::NQ * C::BM) - 1;
+    long long kv_end = p.Sk, kv_begin = 0;
+    if (p.has_hi) kv_end = min(kv_end, (long long)last_row + off + p.hi_off + 1);
+    if (p.has_lo) kv_begin = max(kv_begin, (long long)c.m0 + off - p.win_left);
+    if (kv_end > kv_begin) {
+        c.j0 = (int)(kv_begin / C::BN);
+        c.n_kv = (int)((kv_end + C::BN - 1) / C::BN) - c.j0;
+    } else {
+        c.j0 = 0;
+        c.n_kv = 0;
     }
-    c.n_kv = kv_end > 0 ? (kv_end + C::BN - 1) / C::BN : 0;
     return c;
 }
 
@@ -177,7 +187,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     mbar_arrive_expect_tx(bar(C::kBarKFull + st), C::kKVBytes);
                     for (int a = 0; a < C::DA; ++a)
                         tma_load_4d(sK + st * C::kKVBytes + a * (C::BN * 128), &tm_k,
-                                    bar(C::kBarKFull + st), a * 64, c.hk, j * C::BN, c.b);
+                                    bar(C::kBarKFull + st), a * 64, c.hk, (c.j0 + j) * C::BN, c.b);
                     ok = mbar_wait(bar(C::kBarVEmpty + st), ph, wc);
                     if (!ok) {
                         // K of this iteration is in flight: account for it in the drain
@@ -187,7 +197,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     mbar_arrive_expect_tx(bar(C::kBarVFull + st), C::kKVBytes);
                     for (int a = 0; a < C::DA; ++a)
                         tma_load_4d(sV + st * C::kKVBytes + a * (C::BN * 128), &tm_v,
-                                    bar(C::kBarVFull + st), a * 64, c.hk, j * C::BN, c.b);
+                                    bar(C::kBarVFull + st), a * 64, c.hk, (c.j0 + j) * C::BN, c.b);
                     ++kv_it;
                 }
                 ++tcount;
@@ -360,17 +370,20 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 #pragma unroll
                 for (int ch = 1; ch < kSC; ++ch) reg_fence(u[ch]);
 
-                const int n0 = j * C::BN;
+                const int n0 = (c.j0 + j) * C::BN;
                 const bool need_mask =
-                    (n0 + C::BN > p.Sk) || (p.causal && (n0 + C::BN - 1 > tile_row0 + off));
+                    (n0 + C::BN > p.Sk) ||
+                    (p.has_hi && (n0 + C::BN - 1 > tile_row0 + off + p.hi_off)) ||
+                    (p.has_lo && (n0 < tile_row0 + C::BM - 1 + off - p.win_left));
                 if (need_mask) {
                     int kmax = p.Sk - 1 - n0;
-                    if (p.causal) kmax = min(kmax, row + off - n0);
+                    if (p.has_hi) kmax = min(kmax, row + off + p.hi_off - n0);
+                    const int kmin = p.has_lo ? row + off - p.win_left - n0 : -1;
 #pragma unroll
                     for (int ch = 0; ch < kSC; ++ch)
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            if (ch * 32 + i > kmax) u[ch][i] = 0xff800000u;  // -inf
+                            if (ch * 32 + i > kmax || ch * 32 + i < kmin) u[ch][i] = 0xff800000u;  // -inf
                 }
                 // Row max over the BN scores: four independent chains of 3-input maxima.
                 auto sv = [&](int k) -> float { return __uint_as_float(u[k >> 5][k & 31]); };
@@ -504,6 +517,10 @@ fa_status launch_fwd_cfg(const FwdArgs& a, cudaStream_t stream) {
     p.Hkv = a.Hkv;
     p.group = a.Hq / a.Hkv;
     p.causal = a.causal ? 1 : 0;
+    p.has_lo = a.window_left >= 0 ? 1 : 0;
+    p.win_left = a.window_left >= 0 ? a.window_left : 0;
+    p.has_hi = (a.causal || a.window_right >= 0) ? 1 : 0;
+    p.hi_off = a.causal ? 0 : (a.window_right >= 0 ? a.window_right : 0);
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.num_qb = (a.Sq + C::NQ * C::BM - 1) / (C::NQ * C::BM);
     const long long tiles = (long long)a.B * a.Hq * p.num_qb;

@@ -21,6 +21,7 @@ struct FwdArgs {
     int B, Sq, Sk, Hq, Hkv, D;
     float scale;
     int causal;
+    int window_left, window_right;  // -1: unbounded
     bool bf16;
     int num_sms;
     int* dev_status;
@@ -39,6 +40,8 @@ struct DecodeArgs {
     int num_splits;
     float* o_part;    // [B, Hq, num_splits, D]
     float* lse_part;  // [B, Hq, num_splits]
+    const int32_t* block_table;  // null for a contiguous cache
+    int num_pages, page_size, max_pages;  // paged pool (Smax = page_size * max_pages)
     bool bf16;
     int num_sms;
     int* dev_status;

@@ -81,6 +81,21 @@ FA_API fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, fl
                  fa_stream_t stream);
 
 /*
+ * fa_fwd restricted to a sliding window (local attention; page "flash-attention-v100",
+ * flash_attn_func window_size, and "Changelog", "2.3: Local (i.e., sliding window)
+ * attention"): query i attends only to keys j with
+ *     i + Sk - Sq - window_left <= j <= i + Sk - Sq + window_right,
+ * where -1 leaves that side unbounded; with causal != 0 the right bound is additionally
+ * j <= i + Sk - Sq.  K/V blocks outside every row's window are skipped, not masked.  A row
+ * whose window holds no key gets O = 0 and LSE = -inf.  window_left/right >= -1, else
+ * FA_ERR_INVALID_ARG; everything else as fa_fwd (which equals window (-1, -1)).
+ */
+FA_API fa_status fa_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse,
+                               int B, int Sq, int Sk, int Hq, int Hkv, int D, float scale,
+                               int causal, int window_left, int window_right, fa_dtype dtype,
+                               fa_stream_t stream);
+
+/*
  * Bytes of decode workspace fa_decode_splitkv needs for these sizes and `num_splits`
  * (the partial outputs [B, Hq, num_splits, D] fp32 and their log-sum-exps
  * [B, Hq, num_splits] fp32, each region 256-byte aligned).  0 for invalid sizes.
@@ -109,7 +124,7 @@ FA_API int fa_decode_default_splits(int B, int Hkv, int max_kv_len, int num_sms)
  *            chunk is one work item, and a second kernel merges each sequence's chunks.
  *   workspace   device memory of at least fa_decode_workspace_bytes(B, Hq, D, num_splits)
  *            bytes (after the default is applied); its contents need no initialisation.
- * Sizes: B, Hq, Hkv, Smax >= 1; D == 128 or 64; Hq % Hkv == 0; Hq / Hkv <= 16.
+ * Sizes: B, Hq, Hkv, Smax >= 1; B <= 1024; D == 128; Hq % Hkv == 0; Hq / Hkv <= 16.
  * The result does not depend on num_splits beyond fp32 rounding.  Values of kv_lens
  * outside [0, Smax] are the caller's error and are clamped on the device.
  */
@@ -117,6 +132,27 @@ FA_API fa_status fa_decode_splitkv(const void *q, const void *k_cache, const voi
                             const int32_t *kv_lens, void *o, float *lse, int B, int Hq, int Hkv,
                             int D, int Smax, float scale, int num_splits, void *workspace,
                             size_t workspace_bytes, fa_dtype dtype, fa_stream_t stream);
+
+/*
+ * fa_decode_splitkv over a paged KV cache (page "flash-attention-v100",
+ * flash_attn_with_kvcache with block_table; "Changelog", "2.5: Paged KV cache").
+ *   k_pages, v_pages   [num_pages, page_size, Hkv, D] (dtype): a pool of pages
+ *   block_table        device int32 [B, max_pages_per_seq]: key r of sequence b is row
+ *                      r % page_size of page block_table[b][r / page_size]
+ *   kv_lens            device int32 [B], 0 <= kv_lens[b] <= page_size * max_pages_per_seq
+ * page_size must be a multiple of 128 (the pages ask for multiples of 256, which are
+ * accepted).  Table entries outside [0, num_pages) for pages a sequence uses are the
+ * caller's error: those keys read as zeros, never outside the pool.  Everything else,
+ * including the workspace (fa_decode_workspace_bytes(B, Hq, D, num_splits)) and the
+ * chunking, is as fa_decode_splitkv with Smax = page_size * max_pages_per_seq.
+ */
+FA_API fa_status fa_decode_splitkv_paged(const void *q, const void *k_pages, const void *v_pages,
+                                         const int32_t *block_table, const int32_t *kv_lens,
+                                         void *o, float *lse, int B, int Hq, int Hkv, int D,
+                                         int num_pages, int page_size, int max_pages_per_seq,
+                                         float scale, int num_splits, void *workspace,
+                                         size_t workspace_bytes, fa_dtype dtype,
+                                         fa_stream_t stream);
 
 /*
  * Split-KV decode for callers that cannot allocate device memory -- for example a plugin
