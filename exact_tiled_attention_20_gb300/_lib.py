@@ -279,3 +279,43 @@ def fa_decode_splitkv_paged(q, k_pages, v_pages, block_table, kv_lens, scale: fl
     if st != FA_OK:
         raise FaError(st, "fa_decode_splitkv_paged")
     return out, lse
+
+
+_varlen_declared = False
+
+
+def fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool = False,
+                  scale: float | None = None, window=(-1, -1), out=None, lse=None, stream=None):
+    """Variable-length batch through fa_fwd_varlen: q [total_q, Hq, D], k/v [total_k, Hkv, D],
+    cu_seqlens_q/k int32 [B+1] on the device.  Returns (o [total_q, Hq, D], lse [Hq, total_q])."""
+    global _varlen_declared
+    lib = load()
+    if not _varlen_declared:
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.fa_fwd_varlen.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, I, I, P]
+        lib.fa_fwd_varlen.restype = I
+        _varlen_declared = True
+    if q.dtype not in _DTYPE:
+        raise TypeError("q/k/v must be bf16 or fp16")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_cuda(name, t, q.dtype)
+    _check_cuda("cu_seqlens_q", cu_seqlens_q, torch.int32)
+    _check_cuda("cu_seqlens_k", cu_seqlens_k, torch.int32)
+    total_q, Hq, D = q.shape
+    total_k, Hkv, _ = k.shape
+    B = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have B + 1 entries")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+    with torch.cuda.device(q.device):
+        st = lib.fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               lse.data_ptr(), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B,
+                               total_q, total_k, Hq, Hkv, D, sc, int(bool(causal)), int(window[0]),
+                               int(window[1]), _DTYPE[q.dtype], _stream_handle(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_varlen")
+    return out, lse

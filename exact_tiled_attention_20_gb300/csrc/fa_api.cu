@@ -128,7 +128,40 @@ fa_status fa_fwd_window(const void* q, const void* k, const void* v, void* o, fl
     DeviceInfo di;
     if (!device_info(&di)) return FA_ERR_CUDA;
     FwdArgs a{q, k, v, o, lse, B, Sq, Sk, Hq, Hkv, D, scale, causal, window_left, window_right,
-              dtype == FA_BF16, di.num_sms, di.status};
+              nullptr, nullptr, 0, 0, dtype == FA_BF16, di.num_sms, di.status};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    switch (D) {
+        case 64: return launch_fwd_d64(a, s);
+        case 96: return launch_fwd_d96(a, s);
+        case 128: return launch_fwd_d128(a, s);
+        default: return launch_fwd_d256(a, s);
+    }
+}
+
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int B,
+                        int total_q, int total_k, int Hq, int Hkv, int D, float scale, int causal,
+                        int window_left, int window_right, fa_dtype dtype, fa_stream_t stream) {
+    if (!q || !k || !v || !o || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) ||
+        (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u))
+        return FA_ERR_INVALID_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_INVALID_ARG;
+    if (B <= 0 || total_q <= 0 || total_k <= 0 || Hq <= 0 || Hkv <= 0) return FA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
+    if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_UNSUPPORTED;
+    if (D != 64 && D != 96 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
+    if (B > 1024) return FA_ERR_UNSUPPORTED;
+    if ((long long)total_q * Hq > 0x7fffffffLL || (long long)total_k * Hkv > 0x7fffffffLL)
+        return FA_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    if (!device_info(&di)) return FA_ERR_CUDA;
+    FwdArgs a{q, k, v, o, lse, B, 0, 0, Hq, Hkv, D, scale, causal, window_left, window_right,
+              cu_seqlens_q, cu_seqlens_k, total_q, total_k, dtype == FA_BF16, di.num_sms,
+              di.status};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     switch (D) {
         case 64: return launch_fwd_d64(a, s);

@@ -42,11 +42,27 @@ struct FwdParams {
     // whether each bound applies (hi_off = 0 under the causal flag).
     int has_lo, win_left, has_hi, hi_off;
     float scale_log2;  // softmax scale * log2(e)
-    int num_qb;        // query blocks of NQ * 128 rows per (b, h)
-    int num_tiles;     // B * Hq * num_qb
+    int num_qb;        // query blocks of NQ * 128 rows per (b, h) (fixed-length batches)
+    int num_tiles;     // B * Hq * num_qb (fixed-length batches)
+    // Variable-length batches (page "flash-attention-v100", "Changelog", "2.0",
+    // flash_attn_varlen_func): sequence b holds query rows [cu_q[b], cu_q[b+1]) of a packed
+    // [total_q, Hq, D] tensor and key rows [cu_k[b], cu_k[b+1]) of [total_k, Hkv, D];
+    // null for fixed-length [B, S, H, D] batches.  LSE is then [Hq, total_q].
+    const int32_t* cu_q;
+    const int32_t* cu_k;
+    int total_q;
     void* o;           // [B, Sq, Hq, D]
     float* lse;        // [B, Hq, Sq] or null
     int* status;       // sticky device status word
+};
+
+constexpr int kMaxVarlenB = 1024;
+
+// Work-tile table of a variable-length batch, built by every CTA at start.
+struct VarlenTable {
+    int prefix[kMaxVarlenB + 1];  // exclusive prefix of Hq * ceil(Sq_b / (NQ * 128))
+    int q0[kMaxVarlenB + 1];      // cu_seqlens_q
+    int k0[kMaxVarlenB + 1];      // cu_seqlens_k
 };
 
 template <int D_, int BN_, int NQ_, int NS_>
@@ -84,28 +100,63 @@ struct FwdConfig {
     static constexpr int kBarFinal = kBarODrained + NQ;
     static constexpr int kNumBars = kBarFinal + 1;
     static constexpr int kTileBytes = NQ * kQBytes + 2 * NS * kKVBytes;
-    static constexpr int kSmemBytes = 1024 /* alignment slack */ + kTileBytes + 8 * kNumBars + 16;
+    static constexpr int kSmemBytes =
+        1024 /* alignment slack */ + kTileBytes + 8 * kNumBars + 16 + (int)sizeof(VarlenTable);
     static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
 struct TileCoord {
     int b, h, hk, m0, j0, n_kv;  // K/V blocks j0 .. j0 + n_kv - 1
+    int sq, sk;                  // this sequence's query and key lengths
+    int q_base, k_base, tb;      // TMA row offsets and outer coordinate of the sequence
+    long long o_row0;            // packed output row of query 0 of this sequence
+    long long lse0;              // LSE index of (this sequence, this head, query 0)
 };
 
 template <class C>
-__device__ __forceinline__ TileCoord decode_tile(const FwdParams& p, int t) {
+__device__ __forceinline__ TileCoord decode_tile(const FwdParams& p, const VarlenTable* vt, int t) {
     TileCoord c;
-    const int qb_raw = t % p.num_qb;
-    const int bh = t / p.num_qb;
+    int qb_raw, bh_local, nqb;
+    if (vt) {
+        int lo = 0, hi = p.B;  // largest b with prefix[b] <= t
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (vt->prefix[mid] <= t) lo = mid; else hi = mid;
+        }
+        c.b = lo;
+        c.sq = vt->q0[lo + 1] - vt->q0[lo];
+        c.sk = vt->k0[lo + 1] - vt->k0[lo];
+        nqb = (c.sq + C::NQ * C::BM - 1) / (C::NQ * C::BM);
+        const int local = t - vt->prefix[lo];
+        qb_raw = local % nqb;
+        bh_local = local / nqb;
+        c.h = bh_local;
+        c.q_base = vt->q0[lo];
+        c.k_base = vt->k0[lo];
+        c.tb = 0;
+        c.o_row0 = vt->q0[lo];
+        c.lse0 = (long long)c.h * p.total_q + vt->q0[lo];
+    } else {
+        nqb = p.num_qb;
+        qb_raw = t % nqb;
+        const int bh = t / nqb;
+        c.h = bh % p.Hq;
+        c.b = bh / p.Hq;
+        c.sq = p.Sq;
+        c.sk = p.Sk;
+        c.q_base = 0;
+        c.k_base = 0;
+        c.tb = c.b;
+        c.o_row0 = (long long)c.b * p.Sq;
+        c.lse0 = ((long long)c.b * p.Hq + c.h) * p.Sq;
+    }
     // causal: the longest query block of each head first
-    const int qb = p.causal ? (p.num_qb - 1 - qb_raw) : qb_raw;
-    c.h = bh % p.Hq;
-    c.b = bh / p.Hq;
+    const int qb = p.causal ? (nqb - 1 - qb_raw) : qb_raw;
     c.hk = c.h / p.group;
     c.m0 = qb * (C::NQ * C::BM);
-    const int off = p.Sk - p.Sq;
-    const int last_row = min(p.Sq, c.m0 + C::NQ * C::BM) - 1;
-    long long kv_end = p.Sk, kv_begin = 0;
+    const int off = c.sk - c.sq;
+    const int last_row = min(c.sq, c.m0 + C::NQ * C::BM) - 1;
+    long long kv_end = c.sk, kv_begin = 0;
     if (p.has_hi) kv_end = min(kv_end, (long long)last_row + off + p.hi_off + 1);
     if (p.has_lo) kv_begin = max(kv_begin, (long long)c.m0 + off - p.win_left);
     if (kv_end > kv_begin) {
@@ -133,6 +184,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const uint32_t sBar = sV + C::NS * C::kKVBytes;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_gen + C::kTileBytes + 8 * C::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    VarlenTable* vtab = p.cu_q ? reinterpret_cast<VarlenTable*>(tmem_slot + 4) : nullptr;
     auto bar = [&](int i) -> uint32_t { return sBar + 8u * (uint32_t)i; };
 
     const int warp = threadIdx.x >> 5;
@@ -158,9 +210,27 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
     }
+    int num_tiles = p.num_tiles;
+    if (vtab) {
+        for (int i = threadIdx.x; i <= p.B; i += blockDim.x) {
+            vtab->q0[i] = p.cu_q[i];
+            vtab->k0[i] = p.cu_k[i];
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {  // B <= 1024: a serial scan is a few microseconds at most
+            int run = 0;
+            for (int b = 0; b < p.B; ++b) {
+                vtab->prefix[b] = run;
+                const int sq = max(vtab->q0[b + 1] - vtab->q0[b], 0);
+                run += p.Hq * ((sq + C::NQ * C::BM - 1) / (C::NQ * C::BM));
+            }
+            vtab->prefix[p.B] = run;
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (vtab) num_tiles = vtab->prefix[p.B];
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
     if (warp == C::kProducerWarp) {
@@ -168,8 +238,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         if (lane == 0) {
             uint32_t kv_it = 0, tcount = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-                const TileCoord c = decode_tile<C>(p, t);
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const TileCoord c = decode_tile<C>(p, vtab, t);
                 if (c.n_kv == 0) continue;
                 for (int q = 0; q < C::NQ && ok; ++q) {
                     ok = mbar_wait(bar(C::kBarQEmpty + q), (tcount & 1u) ^ 1u, wc);
@@ -177,7 +247,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     mbar_arrive_expect_tx(bar(C::kBarQFull + q), C::kQBytes);
                     for (int a = 0; a < C::DA; ++a)
                         tma_load_4d(sQ + q * C::kQBytes + a * (C::BM * 128), &tm_q,
-                                    bar(C::kBarQFull + q), a * 64, c.h, c.m0 + q * C::BM, c.b);
+                                    bar(C::kBarQFull + q), a * 64, c.h, c.q_base + c.m0 + q * C::BM, c.tb);
                 }
                 for (int j = 0; j < c.n_kv && ok; ++j) {
                     const uint32_t st = kv_it % C::NS;
@@ -187,7 +257,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     mbar_arrive_expect_tx(bar(C::kBarKFull + st), C::kKVBytes);
                     for (int a = 0; a < C::DA; ++a)
                         tma_load_4d(sK + st * C::kKVBytes + a * (C::BN * 128), &tm_k,
-                                    bar(C::kBarKFull + st), a * 64, c.hk, (c.j0 + j) * C::BN, c.b);
+                                    bar(C::kBarKFull + st), a * 64, c.hk, c.k_base + (c.j0 + j) * C::BN, c.tb);
                     ok = mbar_wait(bar(C::kBarVEmpty + st), ph, wc);
                     if (!ok) {
                         // K of this iteration is in flight: account for it in the drain
@@ -197,7 +267,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     mbar_arrive_expect_tx(bar(C::kBarVFull + st), C::kKVBytes);
                     for (int a = 0; a < C::DA; ++a)
                         tma_load_4d(sV + st * C::kKVBytes + a * (C::BN * 128), &tm_v,
-                                    bar(C::kBarVFull + st), a * 64, c.hk, (c.j0 + j) * C::BN, c.b);
+                                    bar(C::kBarVFull + st), a * 64, c.hk, c.k_base + (c.j0 + j) * C::BN, c.tb);
                     ++kv_it;
                 }
                 ++tcount;
@@ -256,8 +326,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 return C::NQ == 1 ? (iter & 1u) : (uint32_t)q;
             };
 
-            for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-                const TileCoord c = decode_tile<C>(p, t);
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const TileCoord c = decode_tile<C>(p, vtab, t);
                 const int n = c.n_kv;
                 if (n == 0) continue;
                 for (int q = 0; q < C::NQ && ok; ++q) ok = mbar_wait(bar(C::kBarQFull + q), tcount & 1u, wc);
@@ -333,21 +403,24 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         const float kNegInf = -__int_as_float(0x7f800000);
         constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
         constexpr int kSC = C::BN / 32;        // 32-column chunks of S per block
-        const int off = p.Sk - p.Sq;           // bottom-right causal alignment
         const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
         uint32_t it = 0, tcount = 0;
         bool ok = true;
 
-        for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-            const TileCoord c = decode_tile<C>(p, t);
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            const TileCoord c = decode_tile<C>(p, vtab, t);
             const int row = c.m0 + q * C::BM + r;
-            const size_t o_row = ((size_t)c.b * p.Sq + row) * p.Hq + c.h;
+            const int off = c.sk - c.sq;  // bottom-right causal alignment
+            // Rows are stored only inside the sequence and inside the packed tensor (the
+            // second test guards against malformed cu_seqlens of a variable-length batch).
+            const bool row_ok = row < c.sq && c.o_row0 + row >= 0 && c.o_row0 + row < p.total_q;
+            const size_t o_row = (size_t)(c.o_row0 + row) * p.Hq + c.h;
             uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + o_row * C::D;
             if (c.n_kv == 0) {
-                if (row < p.Sq) {
+                if (row_ok) {
 #pragma unroll
                     for (int d = 0; d < C::D; d += 8) st_global_v4(orow + d, 0u, 0u, 0u, 0u);
-                    if (p.lse) p.lse[((size_t)c.b * p.Hq + c.h) * p.Sq + row] = kNegInf;
+                    if (p.lse) p.lse[c.lse0 + row] = kNegInf;
                 }
                 continue;
             }
@@ -372,11 +445,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
 
                 const int n0 = (c.j0 + j) * C::BN;
                 const bool need_mask =
-                    (n0 + C::BN > p.Sk) ||
+                    (n0 + C::BN > c.sk) ||
                     (p.has_hi && (n0 + C::BN - 1 > tile_row0 + off + p.hi_off)) ||
                     (p.has_lo && (n0 < tile_row0 + C::BM - 1 + off - p.win_left));
                 if (need_mask) {
-                    int kmax = p.Sk - 1 - n0;
+                    int kmax = c.sk - 1 - n0;
                     if (p.has_hi) kmax = min(kmax, row + off + p.hi_off - n0);
                     const int kmin = p.has_lo ? row + off - p.win_left - n0 : -1;
 #pragma unroll
@@ -473,7 +546,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 for (int i = 0; i < 16; ++i)
                     w[i] = pack2<kBF16>(__uint_as_float(ov[2 * i]) * inv_l,
                                         __uint_as_float(ov[2 * i + 1]) * inv_l);
-                if (row < p.Sq) {
+                if (row_ok) {
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4)
                         st_global_v4(orow + ch * 32 + v4 * 8, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
@@ -483,10 +556,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::kBarODrained + q));
-            if (p.lse && row < p.Sq) {
+            if (p.lse && row_ok) {
                 const float lse = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.69314718055994531f
                                                 : kNegInf;
-                p.lse[((size_t)c.b * p.Hq + c.h) * p.Sq + row] = lse;
+                p.lse[c.lse0 + row] = lse;
             }
         }
     }
@@ -505,9 +578,15 @@ fa_status launch_fwd_cfg(const FwdArgs& a, cudaStream_t stream) {
     static int attr_bf16[64] = {0};
     static int attr_f16[64] = {0};
     CUtensorMap tq, tk, tv;
-    if (!encode_tmap_4d(&tq, a.q, a.bf16, a.D, a.Hq, a.Sq, a.B, C::BM) ||
-        !encode_tmap_4d(&tk, a.k, a.bf16, a.D, a.Hkv, a.Sk, a.B, C::BN) ||
-        !encode_tmap_4d(&tv, a.v, a.bf16, a.D, a.Hkv, a.Sk, a.B, C::BN))
+    const bool varlen = a.cu_q != nullptr;
+    // Fixed-length batches map [B, S, H, D] as (D, H, S, B); packed variable-length
+    // batches map [total, H, D] as (D, H, total, 1).
+    const uint64_t q_rows = varlen ? (uint64_t)a.total_q : (uint64_t)a.Sq;
+    const uint64_t k_rows = varlen ? (uint64_t)a.total_k : (uint64_t)a.Sk;
+    const uint64_t outer = varlen ? 1 : (uint64_t)a.B;
+    if (!encode_tmap_4d(&tq, a.q, a.bf16, a.D, a.Hq, q_rows, outer, C::BM) ||
+        !encode_tmap_4d(&tk, a.k, a.bf16, a.D, a.Hkv, k_rows, outer, C::BN) ||
+        !encode_tmap_4d(&tv, a.v, a.bf16, a.D, a.Hkv, k_rows, outer, C::BN))
         return FA_ERR_CUDA;
     FwdParams p;
     p.B = a.B;
@@ -522,14 +601,23 @@ fa_status launch_fwd_cfg(const FwdArgs& a, cudaStream_t stream) {
     p.has_hi = (a.causal || a.window_right >= 0) ? 1 : 0;
     p.hi_off = a.causal ? 0 : (a.window_right >= 0 ? a.window_right : 0);
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    p.num_qb = (a.Sq + C::NQ * C::BM - 1) / (C::NQ * C::BM);
-    const long long tiles = (long long)a.B * a.Hq * p.num_qb;
-    if (tiles > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-    p.num_tiles = (int)tiles;
+    p.cu_q = a.cu_q;
+    p.cu_k = a.cu_k;
+    p.total_q = varlen ? a.total_q : a.B * a.Sq;  // packed rows of O (the store guard)
+    int grid = a.num_sms;
+    if (!varlen) {
+        p.num_qb = (a.Sq + C::NQ * C::BM - 1) / (C::NQ * C::BM);
+        const long long tiles = (long long)a.B * a.Hq * p.num_qb;
+        if (tiles > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+        p.num_tiles = (int)tiles;
+        grid = p.num_tiles < a.num_sms ? p.num_tiles : a.num_sms;
+    } else {
+        p.num_qb = 0;
+        p.num_tiles = 0;  // counted on the device from cu_seqlens
+    }
     p.o = a.o;
     p.lse = a.lse;
     p.status = a.dev_status;
-    const int grid = p.num_tiles < a.num_sms ? p.num_tiles : a.num_sms;
     auto kern = a.bf16 ? fa_fwd_kernel<C, true> : fa_fwd_kernel<C, false>;
     if (!ensure_smem_attr((const void*)kern, C::kSmemBytes, a.bf16 ? attr_bf16 : attr_f16))
         return FA_ERR_CUDA;

@@ -22,6 +22,9 @@ struct FwdArgs {
     float scale;
     int causal;
     int window_left, window_right;  // -1: unbounded
+    const int32_t* cu_q;            // variable-length batch: null for [B, S, H, D]
+    const int32_t* cu_k;
+    int total_q, total_k;
     bool bf16;
     int num_sms;
     int* dev_status;

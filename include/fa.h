@@ -96,6 +96,25 @@ FA_API fa_status fa_fwd_window(const void *q, const void *k, const void *v, void
                                fa_stream_t stream);
 
 /*
+ * Variable-length batch (page "flash-attention-v100", "Changelog", "2.0",
+ * flash_attn_varlen_func): the B sequences are packed along the rows.
+ *   q, o          [total_q, Hq, D]     k, v  [total_k, Hkv, D]      (dtype)
+ *   cu_seqlens_q  device int32 [B + 1]: sequence b owns query rows
+ *                 [cu_seqlens_q[b], cu_seqlens_q[b + 1]); cu_seqlens_k likewise for keys;
+ *                 both non-decreasing, from 0, ending at most at total_q / total_k.
+ *   lse           [Hq, total_q] fp32 (may be NULL).
+ * Within a sequence everything is as fa_fwd_window: the causal mask is aligned to that
+ * sequence's bottom-right corner.  A sequence with no keys gets O = 0 and LSE = -inf.
+ * B <= 1024.  The offsets are read on the device; rows they place outside [0, total_q)
+ * are not written, and keys outside [0, total_k) read as zero.
+ */
+FA_API fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                               const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int B,
+                               int total_q, int total_k, int Hq, int Hkv, int D, float scale,
+                               int causal, int window_left, int window_right, fa_dtype dtype,
+                               fa_stream_t stream);
+
+/*
  * Bytes of decode workspace fa_decode_splitkv needs for these sizes and `num_splits`
  * (the partial outputs [B, Hq, num_splits, D] fp32 and their log-sum-exps
  * [B, Hq, num_splits] fp32, each region 256-byte aligned).  0 for invalid sizes.

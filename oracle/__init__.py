@@ -19,6 +19,8 @@ the pages as cited in that file's header:
   is the exact identity over a partition of the key set).
 * ``decode_paged`` -- decode over a paged KV cache addressed through a block table
   (flash_attn_with_kvcache block_table; "Changelog", "2.5: Paged KV cache").
+* ``fwd_varlen`` -- variable-length batches: independent sequences packed along rows
+  (flash_attn_varlen_func; "Changelog", "2.0").
 * ``fwd(..., window=(left, right))`` -- sliding-window local attention (page
   "flash-attention-v100", flash_attn_func window_size; "Changelog", "2.3").
 
@@ -226,4 +228,28 @@ def decode_paged(q, k_pages, v_pages, block_table, kv_lens, scale: float, nthrea
                                         float(scale), _ptr(o), _ptr(lse), _threads(nthreads))
     if rc:
         raise ValueError(f"fa_oracle_decode_paged failed with code {rc}")
+    return o, lse
+
+
+def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool = False,
+               window=(-1, -1), nthreads=None):
+    """Variable-length batch (flash_attn_varlen_func; page "flash-attention-v100",
+    "Changelog", "2.0"): sequence b is the independent attention problem over query rows
+    cu_q[b]:cu_q[b+1] and key rows cu_k[b]:cu_k[b+1] of packed [total, H, D] tensors.
+    Returns o [total_q, Hq, D] and lse [Hq, total_q], fp64."""
+    cq = [int(x) for x in np.asarray(cu_seqlens_q).reshape(-1)]
+    ck = [int(x) for x in np.asarray(cu_seqlens_k).reshape(-1)]
+    total_q, Hq, D = q.shape
+    o = np.zeros((total_q, Hq, D), np.float64)
+    lse = np.full((Hq, total_q), -np.inf)
+    for b in range(len(cq) - 1):
+        sq, sk = cq[b + 1] - cq[b], ck[b + 1] - ck[b]
+        if sq <= 0:
+            continue
+        if sk <= 0:
+            continue  # no keys: zero output, -inf log-sum-exp
+        ob, lb = fwd(q[None, cq[b]:cq[b + 1]], k[None, ck[b]:ck[b + 1]], v[None, ck[b]:ck[b + 1]],
+                     scale=scale, causal=causal, window=window, nthreads=nthreads)
+        o[cq[b]:cq[b + 1]] = ob[0]
+        lse[:, cq[b]:cq[b + 1]] = lb[0]
     return o, lse

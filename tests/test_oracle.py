@@ -412,3 +412,27 @@ def test_paged_rejects_out_of_pool_pages():
     table[0, 1] = 99
     with pytest.raises(ValueError):
         oracle.decode_paged(q, k_pages, k_pages, table, lens, scale=0.4)
+
+
+# ------------------------------------------------------------- varlen batches ----
+
+def test_varlen_with_equal_lengths_equals_batched():
+    q, k, v = _rand(3, 7, 4, 8), _rand(3, 9, 2, 8), _rand(3, 9, 2, 8)
+    o_b, l_b = oracle.fwd(q, k, v, scale=0.5, causal=True)
+    o_v, l_v = oracle.fwd_varlen(q.reshape(21, 4, 8), k.reshape(27, 2, 8), v.reshape(27, 2, 8),
+                                 [0, 7, 14, 21], [0, 9, 18, 27], scale=0.5, causal=True)
+    assert np.array_equal(o_v.reshape(3, 7, 4, 8), o_b)
+    assert np.array_equal(l_v.reshape(4, 3, 7).transpose(1, 0, 2), l_b)
+
+
+def test_varlen_sequences_are_independent_and_empty_ones_are_zero():
+    q, k, v = _rand(10, 2, 8), _rand(12, 1, 8), _rand(12, 1, 8)
+    cq, ck = [0, 4, 4, 10], [0, 5, 9, 9]  # sequence 1 has no queries, sequence 2 no keys
+    o, lse = oracle.fwd_varlen(q, k, v, cq, ck, scale=0.7)
+    o0, l0 = oracle.fwd(q[None, 0:4], k[None, 0:5], v[None, 0:5], scale=0.7)
+    assert np.array_equal(o[0:4], o0[0]) and np.array_equal(lse[:, 0:4], l0[0])
+    assert np.all(o[4:10] == 0) and np.all(lse[:, 4:10] == -np.inf)
+    k2 = k.copy()
+    k2[5:] += 3.0  # other sequences' keys do not touch sequence 0
+    o2, _ = oracle.fwd_varlen(q, k2, v, cq, ck, scale=0.7)
+    assert np.array_equal(o2[0:4], o[0:4])
