@@ -319,3 +319,49 @@ def fa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal: bool = False,
     if st != FA_OK:
         raise FaError(st, "fa_fwd_varlen")
     return out, lse
+
+
+_multi_declared = False
+
+
+def fa_decode_splitkv_multi(q, k_cache, v_cache, kv_lens, causal: bool = True,
+                            scale: float | None = None, num_splits: int = 0, workspace=None,
+                            out=None, lse=None, stream=None):
+    """Several query tokens per sequence through fa_decode_splitkv_multi.
+    q [B, Sq, Hq, D]; returns (o [B, Sq, Hq, D], lse [B, Hq, Sq])."""
+    global _multi_declared
+    lib = load()
+    if not _multi_declared:
+        P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.fa_decode_splitkv_multi.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, SZ,
+                                                I, P]
+        lib.fa_decode_splitkv_multi.restype = I
+        _multi_declared = True
+    if q.dtype not in _DTYPE:
+        raise TypeError("q/k_cache/v_cache must be bf16 or fp16")
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _check_cuda(name, t, q.dtype)
+    _check_cuda("kv_lens", kv_lens, torch.int32)
+    B, Sq, Hq, D = q.shape
+    _, Smax, Hkv, _ = k_cache.shape
+    with torch.cuda.device(q.device):
+        ns = int(num_splits) if num_splits and num_splits > 0 else \
+            lib.fa_decode_default_splits(B, Hkv, Smax, 0)
+        ns = min(ns, Smax)
+        if workspace is None:
+            workspace = torch.empty(lib.fa_decode_workspace_bytes(B * Sq, Hq, D, ns),
+                                    dtype=torch.uint8, device=q.device)
+        if out is None:
+            out = torch.empty_like(q)
+        if lse is None:
+            lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+        sc = float(scale) if scale is not None else 1.0 / math.sqrt(D)
+        st = lib.fa_decode_splitkv_multi(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                         kv_lens.data_ptr(), out.data_ptr(), lse.data_ptr(), B, Sq,
+                                         Hq, Hkv, D, Smax, sc, int(bool(causal)), ns,
+                                         workspace.data_ptr(),
+                                         workspace.numel() * workspace.element_size(),
+                                         _DTYPE[q.dtype], _stream_handle(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_decode_splitkv_multi")
+    return out, lse

@@ -209,9 +209,10 @@ namespace {
 // Shared validation and dispatch of the contiguous and paged decode entry points.
 fa_status decode_common(const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* block_table, const int32_t* kv_lens, void* o, float* lse,
-                        int B, int Hq, int Hkv, int D, int Smax, int num_pages, int page_size,
-                        int max_pages, float scale, int num_splits, void* workspace,
-                        size_t workspace_bytes, fa_dtype dtype, fa_stream_t stream) {
+                        int B, int Sq, int Hq, int Hkv, int D, int Smax, int num_pages,
+                        int page_size, int max_pages, float scale, int causal, int num_splits,
+                        void* workspace, size_t workspace_bytes, fa_dtype dtype,
+                        fa_stream_t stream) {
     if (!q || !k_cache || !v_cache || !kv_lens || !o) return FA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
         (reinterpret_cast<uintptr_t>(kv_lens) & 3u))
@@ -222,20 +223,21 @@ fa_status decode_common(const void* q, const void* k_cache, const void* v_cache,
     if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
     if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_UNSUPPORTED;
     if (D != 128) return FA_ERR_UNSUPPORTED;
-    if (Hq / Hkv > 16 || B > 1024) return FA_ERR_UNSUPPORTED;
+    if (Sq <= 0) return FA_ERR_INVALID_ARG;
+    if ((Hq / Hkv) * Sq > 16 || B > 1024) return FA_ERR_UNSUPPORTED;
     if ((long long)B * Smax > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
     DeviceInfo di;
     if (!device_info(&di)) return FA_ERR_CUDA;
     if (num_splits <= 0) num_splits = fa_decode_default_splits(B, Hkv, Smax, di.num_sms);
     if (num_splits > Smax) num_splits = Smax;
-    const size_t need = fa_decode_workspace_bytes(B, Hq, D, num_splits);
+    const size_t need = fa_decode_workspace_bytes(B * Sq, Hq, D, num_splits);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return FA_ERR_WORKSPACE;
-    const size_t rows = (size_t)B * Hq * num_splits;
+    const size_t rows = (size_t)B * Sq * Hq * num_splits;
     float* o_part = static_cast<float*>(workspace);
     float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                                ((rows * D * sizeof(float) + 255) & ~size_t(255)));
     DecodeArgs a{q, k_cache, v_cache, kv_lens, o, lse, B, Hq, Hkv, D, Smax, scale, num_splits,
-                 o_part, lse_part, block_table, num_pages, page_size, max_pages,
+                 o_part, lse_part, Sq, causal, block_table, num_pages, page_size, max_pages,
                  dtype == FA_BF16, di.num_sms, di.status};
     return launch_decode(a, reinterpret_cast<cudaStream_t>(stream));
 }
@@ -246,8 +248,18 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
                             const int32_t* kv_lens, void* o, float* lse, int B, int Hq, int Hkv,
                             int D, int Smax, float scale, int num_splits, void* workspace,
                             size_t workspace_bytes, fa_dtype dtype, fa_stream_t stream) {
-    return decode_common(q, k_cache, v_cache, nullptr, kv_lens, o, lse, B, Hq, Hkv, D, Smax, 0, 0,
-                         0, scale, num_splits, workspace, workspace_bytes, dtype, stream);
+    return decode_common(q, k_cache, v_cache, nullptr, kv_lens, o, lse, B, 1, Hq, Hkv, D, Smax, 0,
+                         0, 0, scale, 0, num_splits, workspace, workspace_bytes, dtype, stream);
+}
+
+fa_status fa_decode_splitkv_multi(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* kv_lens, void* o, float* lse, int B, int Sq, int Hq,
+                                  int Hkv, int D, int Smax, float scale, int causal, int num_splits,
+                                  void* workspace, size_t workspace_bytes, fa_dtype dtype,
+                                  fa_stream_t stream) {
+    return decode_common(q, k_cache, v_cache, nullptr, kv_lens, o, lse, B, Sq, Hq, Hkv, D, Smax, 0,
+                         0, 0, scale, causal, num_splits, workspace, workspace_bytes, dtype,
+                         stream);
 }
 
 fa_status fa_decode_splitkv_paged(const void* q, const void* k_pages, const void* v_pages,
@@ -261,8 +273,8 @@ fa_status fa_decode_splitkv_paged(const void* q, const void* k_pages, const void
     if (page_size % 128 != 0) return FA_ERR_UNSUPPORTED;
     const long long smax = (long long)page_size * max_pages_per_seq;
     if (smax > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-    return decode_common(q, k_pages, v_pages, block_table, kv_lens, o, lse, B, Hq, Hkv, D,
-                         (int)smax, num_pages, page_size, max_pages_per_seq, scale, num_splits,
+    return decode_common(q, k_pages, v_pages, block_table, kv_lens, o, lse, B, 1, Hq, Hkv, D,
+                         (int)smax, num_pages, page_size, max_pages_per_seq, scale, 0, num_splits,
                          workspace, workspace_bytes, dtype, stream);
 }
 

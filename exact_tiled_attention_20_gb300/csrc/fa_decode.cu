@@ -41,7 +41,11 @@ struct DecParams {
     float* lse_part;  // [B, Hq, ns]
     void* o;          // [B, Hq, D]
     float* lse;       // [B, Hq] or null
-    int q_rows;  // query-head rows per Q box (min(16, Hq)); rows past it are never read
+    int q_rows;  // query-head rows per Q box; rows past q_rows * sq are never read
+    // Several query tokens per sequence (flash_attn_with_kvcache with seqlen_q > 1): the
+    // MMA's N columns hold (token s, head h) as column s * group + h; with `causal` token s
+    // sees keys j <= kv_len - sq + s (bottom-right alignment).  sq = 1 for plain decode.
+    int sq, causal;
     // Paged cache (page "flash-attention-v100", flash_attn_with_kvcache block_table;
     // "Changelog", "2.5: Paged KV cache"): key r of sequence b is row r % page_size of
     // page block_table[b * max_pages + r / page_size]; page_size is a multiple of 128.
@@ -249,7 +253,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 const uint32_t qs = icount & 1u;
                 ok = mbar_wait(bar(kDBarQEmpty + qs), ((icount >> 1) & 1u) ^ 1u, wc);
                 if (!ok) break;
-                mbar_arrive_expect_tx(bar(kDBarQFull + qs), kDecDA * p.q_rows * 128);
+                mbar_arrive_expect_tx(bar(kDBarQFull + qs), kDecDA * p.q_rows * p.sq * 128);
                 for (int a = 0; a < kDecDA; ++a)
                     tma_load_4d(sQ + qs * kDecQBytes + a * 2048, &tm_q, bar(kDBarQFull + qs), a * 64,
                                 it.hk * p.group, 0, it.b);
@@ -400,11 +404,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 uint32_t u[16];
                 tmem_ld_32x32b_x16(lane_base + slot * 16, u);
                 tmem_wait_ld(u);
-                const bool valid = item.k0 + j * kDecBN + tid < item.k1;
+                const int key = item.k0 + j * kDecBN + tid;
+                const bool valid = key < item.k1;
+                const int ncols = g * p.sq;
+                const int lim0 = T.lens[item.b] - p.sq;  // token s sees keys <= lim0 + s
                 float sv[GMAX];
 #pragma unroll
                 for (int h = 0; h < GMAX; ++h) {
-                    sv[h] = (valid && h < g) ? __uint_as_float(u[h]) : kNegInf;
+                    const bool vis = valid && h < ncols && (!p.causal || key <= lim0 + h / g);
+                    sv[h] = vis ? __uint_as_float(u[h]) : kNegInf;
                     float m = sv[h];
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -471,12 +479,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 if (lane == 0) T.lred[warp][h] = s;
             }
             named_bar_sync(1, 128);
-            const size_t row0 = ((size_t)item.b * p.Hq + (size_t)item.hk * g) * p.ns + item.c;
 #pragma unroll
             for (int h = 0; h < GMAX; ++h) {
                 const float lt = (T.lred[0][h] + T.lred[1][h]) + (T.lred[2][h] + T.lred[3][h]);
-                if (h < g) {
-                    const size_t row = row0 + (size_t)h * p.ns;
+                if (h < g * p.sq) {
+                    // column h is (token h / g, head hk * g + h % g); rows are [B, sq, Hq]
+                    const size_t qrow = ((size_t)item.b * p.sq + h / g) * p.Hq + (size_t)item.hk * g + h % g;
+                    const size_t row = qrow * p.ns + item.c;
                     p.o_part[row * kDecD + tid] = lt > 0.f ? __uint_as_float(ov[h]) / lt : 0.f;
                     if (tid == 0)
                         p.lse_part[row] =
@@ -508,9 +517,11 @@ __global__ void __launch_bounds__(128)
     const int per = (s_max_len + p.ns - 1) / p.ns;
     const int L = max(kDecBN, (per + kDecBN - 1) / kDecBN * kDecBN);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x * 4 + warp;
-    if (bh >= p.B * p.Hq) return;
-    const int b = bh / p.Hq;
+    const int bh = blockIdx.x * 4 + warp;  // row of [B, sq, Hq]
+    if (bh >= p.B * p.sq * p.Hq) return;
+    const int b = bh / (p.sq * p.Hq);
+    const int s_tok = (bh / p.Hq) % p.sq;
+    const int hq = bh % p.Hq;
     const int len = min(max(p.kv_lens[b], 0), p.Smax);
     const int n = (len + L - 1) / L;
     const float kNegInf = -__int_as_float(0x7f800000);
@@ -522,11 +533,13 @@ __global__ void __launch_bounds__(128)
     // The partials are written by the split kernel, which may still be running when this
     // grid starts (programmatic dependent launch): wait for its completion here.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (n > 0) {
-        float m = kNegInf;
-        for (int c = lane; c < n; c += 32) m = fmaxf(m, lrow[c]);
+    float m = kNegInf;
+    for (int c = lane; c < n; c += 32) m = fmaxf(m, lrow[c]);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    // m = -inf: no chunk holds a visible key for this row (empty cache, or a causal token
+    // that sees none): O = 0, LSE = -inf.
+    if (n > 0 && m != kNegInf) {
         float s = 0.f;
         for (int c = lane; c < n; c += 32) s += ex2_approx((lrow[c] - m) * kLog2e);
 #pragma unroll
@@ -566,7 +579,7 @@ __global__ void __launch_bounds__(128)
     const uint32_t w0 = pack2<kBF16>(acc[0], acc[1]);
     const uint32_t w1 = pack2<kBF16>(acc[2], acc[3]);
     asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(out), "r"(w0), "r"(w1) : "memory");
-    if (p.lse && lane == 0) p.lse[bh] = lse;
+    if (p.lse && lane == 0) p.lse[((size_t)b * p.Hq + hq) * p.sq + s_tok] = lse;
 }
 
 template <int GMAX, bool kBF16>
@@ -584,11 +597,12 @@ fa_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
     if (a.B > kDecMaxB) return FA_ERR_UNSUPPORTED;
     const int g = a.Hq / a.Hkv;
     CUtensorMap tq, tk, tv;
-    const int q_rows = a.Hq < 16 ? a.Hq : 16;
+    const int g_cols = (a.Hq / a.Hkv) * a.sq;  // MMA N columns in use
+    const int q_rows = a.sq == 1 ? (a.Hq < 16 ? a.Hq : 16) : a.Hq / a.Hkv;
     // Contiguous caches are [B, Smax, Hkv, D]; paged pools are [num_pages, page_size, Hkv, D].
     const uint64_t rows_dim = a.block_table ? (uint64_t)a.page_size : (uint64_t)a.Smax;
     const uint64_t outer_dim = a.block_table ? (uint64_t)a.num_pages : (uint64_t)a.B;
-    if (!encode_tmap_4d_box(&tq, a.q, a.bf16, a.D, a.Hq, 1, a.B, q_rows, 1) ||
+    if (!encode_tmap_4d_box(&tq, a.q, a.bf16, a.D, a.Hq, a.sq, a.B, q_rows, a.sq) ||
         !encode_tmap_4d(&tk, a.k_cache, a.bf16, a.D, a.Hkv, rows_dim, outer_dim, kDecBN) ||
         !encode_tmap_4d(&tv, a.v_cache, a.bf16, a.D, a.Hkv, rows_dim, outer_dim, kDecBN))
         return FA_ERR_CUDA;
@@ -607,15 +621,18 @@ fa_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
     p.lse = a.lse;
     p.status = a.dev_status;
     p.q_rows = q_rows;
+    p.sq = a.sq;
+    p.causal = a.causal ? 1 : 0;
     p.block_table = a.block_table;
     p.page_size = a.page_size;
     p.max_pages = a.max_pages;
     const long long items_max = (long long)a.B * a.Hkv * a.num_splits;
     const int grid = (int)(items_max < a.num_sms ? items_max : a.num_sms);
     fa_status st;
-    if (g <= 4)
+    if (g_cols > 16) return FA_ERR_UNSUPPORTED;
+    if (g_cols <= 4)
         st = a.bf16 ? launch_split<4, true>(tq, tk, tv, p, grid, s) : launch_split<4, false>(tq, tk, tv, p, grid, s);
-    else if (g <= 8)
+    else if (g_cols <= 8)
         st = a.bf16 ? launch_split<8, true>(tq, tk, tv, p, grid, s) : launch_split<8, false>(tq, tk, tv, p, grid, s);
     else
         st = a.bf16 ? launch_split<16, true>(tq, tk, tv, p, grid, s) : launch_split<16, false>(tq, tk, tv, p, grid, s);
@@ -623,7 +640,7 @@ fa_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
     // The merge kernel is launched as a programmatic dependent of the split kernel: its
     // launch overlaps the split kernel's tail, and it waits for the split results itself.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((a.B * a.Hq + 3) / 4));
+    cfg.gridDim = dim3((unsigned)((a.B * a.sq * a.Hq + 3) / 4));
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;

@@ -43,6 +43,7 @@ struct DecodeArgs {
     int num_splits;
     float* o_part;    // [B, Hq, num_splits, D]
     float* lse_part;  // [B, Hq, num_splits]
+    int sq, causal;              // query tokens per sequence (1 = plain decode)
     const int32_t* block_table;  // null for a contiguous cache
     int num_pages, page_size, max_pages;  // paged pool (Smax = page_size * max_pages)
     bool bf16;

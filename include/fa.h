@@ -153,6 +153,24 @@ FA_API fa_status fa_decode_splitkv(const void *q, const void *k_cache, const voi
                             size_t workspace_bytes, fa_dtype dtype, fa_stream_t stream);
 
 /*
+ * Split-KV decode with Sq >= 1 query tokens per sequence (speculative or chunked decoding;
+ * page "flash-attention-v100", flash_attn_with_kvcache with seqlen_q > 1 and the causal
+ * flag of "Changelog", "2.1").
+ *   q, o      [B, Sq, Hq, D] (dtype)     lse [B, Hq, Sq] fp32 (may be NULL)
+ *   causal    nonzero: token s of sequence b sees cache keys j <= kv_lens[b] - Sq + s
+ *             (the bottom-right aligned mask); zero: every token sees [0, kv_lens[b]).
+ * (Hq / Hkv) * Sq <= 16.  The workspace is fa_decode_workspace_bytes(B * Sq, Hq, D,
+ * num_splits).  A token that sees no key gets O = 0 and LSE = -inf.  Everything else as
+ * fa_decode_splitkv, which is the Sq = 1 case.
+ */
+FA_API fa_status fa_decode_splitkv_multi(const void *q, const void *k_cache, const void *v_cache,
+                                         const int32_t *kv_lens, void *o, float *lse, int B,
+                                         int Sq, int Hq, int Hkv, int D, int Smax, float scale,
+                                         int causal, int num_splits, void *workspace,
+                                         size_t workspace_bytes, fa_dtype dtype,
+                                         fa_stream_t stream);
+
+/*
  * fa_decode_splitkv over a paged KV cache (page "flash-attention-v100",
  * flash_attn_with_kvcache with block_table; "Changelog", "2.5: Paged KV cache").
  *   k_pages, v_pages   [num_pages, page_size, Hkv, D] (dtype): a pool of pages

@@ -19,6 +19,8 @@ the pages as cited in that file's header:
   is the exact identity over a partition of the key set).
 * ``decode_paged`` -- decode over a paged KV cache addressed through a block table
   (flash_attn_with_kvcache block_table; "Changelog", "2.5: Paged KV cache").
+* ``decode_multi`` -- several query tokens per sequence over a KV cache, bottom-right
+  causal (flash_attn_with_kvcache with seqlen_q > 1).
 * ``fwd_varlen`` -- variable-length batches: independent sequences packed along rows
   (flash_attn_varlen_func; "Changelog", "2.0").
 * ``fwd(..., window=(left, right))`` -- sliding-window local attention (page
@@ -252,4 +254,25 @@ def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool =
                      scale=scale, causal=causal, window=window, nthreads=nthreads)
         o[cq[b]:cq[b + 1]] = ob[0]
         lse[:, cq[b]:cq[b + 1]] = lb[0]
+    return o, lse
+
+
+def decode_multi(q, k_cache, v_cache, kv_lens, scale: float, causal: bool = True, nthreads=None):
+    """Several query tokens per sequence over a KV cache (flash_attn_with_kvcache with
+    seqlen_q > 1; page "flash-attention-v100", "How to use FlashAttention"): the Sq
+    queries of sequence b attend to cache keys [0, kv_lens[b]), and with ``causal`` the
+    mask is aligned to the bottom-right corner, so query s sees keys
+    j <= kv_lens[b] - Sq + s.  q [B, Sq, Hq, D]; returns o [B, Sq, Hq, D] and
+    lse [B, Hq, Sq] in fp64."""
+    B, Sq, Hq, D = q.shape
+    lens = [int(x) for x in np.asarray(kv_lens).reshape(-1)]
+    o = np.zeros((B, Sq, Hq, D), np.float64)
+    lse = np.full((B, Hq, Sq), -np.inf)
+    for b in range(B):
+        if lens[b] <= 0:
+            continue
+        ob, lb = fwd(q[b:b + 1], k_cache[b:b + 1, :lens[b]], v_cache[b:b + 1, :lens[b]], scale=scale,
+                     causal=causal, nthreads=nthreads)
+        o[b] = ob[0]
+        lse[b] = lb[0]
     return o, lse

@@ -1,0 +1,94 @@
+"""GPU parity of fa_decode_splitkv_multi (split-KV decode with several query tokens).
+
+Semantics: flash_attn_with_kvcache with seqlen_q > 1 (page "flash-attention-v100"), the
+causal mask aligned to the bottom-right corner ("Changelog", "2.1"): token s of sequence
+b sees cache keys j <= kv_lens[b] - Sq + s.  Checked element by element against the fp64
+oracle (oracle.decode_multi) with max|dO| <= 1e-2, max|dLSE| <= 1e-3, for token counts
+1-8, group sizes up to 16 columns, causal and not, and caches shorter than Sq (tokens
+that see no key); Sq = 1 must reproduce fa_decode_splitkv bit for bit.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_tiled_attention_20_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 1e-2
+LSE_TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def fa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import exact_tiled_attention_20_gb300 as fa_mod
+    from exact_tiled_attention_20_gb300 import build
+
+    build.build_library()
+    fa_mod.load()
+    return fa_mod
+
+
+def _make(B, Sq, Hq, Hkv, D, smax, lens, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((B, Sq, Hq, D), generator=g).to(torch.bfloat16)
+    kc = torch.randn((B, smax, Hkv, D), generator=g).to(torch.bfloat16)
+    vc = torch.randn((B, smax, Hkv, D), generator=g).to(torch.bfloat16)
+    return q, kc, vc, torch.tensor(lens, dtype=torch.int32)
+
+
+@pytest.mark.parametrize("Sq,Hq,Hkv,causal,ns", [(2, 8, 2, True, 3), (4, 8, 2, True, 5),
+                                                 (4, 8, 2, False, 2), (8, 4, 2, True, 4),
+                                                 (16, 2, 2, True, 1), (3, 6, 2, True, 7),
+                                                 (2, 16, 2, True, 2)])
+def test_multi_token_decode_matches_oracle(fa, Sq, Hq, Hkv, causal, ns):
+    lens = [1500, 3, 0, 777]
+    q, kc, vc, lens_t = _make(4, Sq, Hq, Hkv, 128, 1600, lens, seed=Sq * 100 + Hq)
+    dev = torch.device("cuda:0")
+    o, lse = fa.fa_decode_splitkv_multi(q.to(dev), kc.to(dev), vc.to(dev), lens_t.to(dev),
+                                        causal=causal, num_splits=ns)
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == 0
+    o_ref, lse_ref = oracle.decode_multi(q, kc, vc, lens, scale=1 / math.sqrt(128), causal=causal)
+    of, lf = o.float().cpu().numpy(), lse.cpu().numpy()
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(fin, np.isfinite(lf)), "LSE -inf pattern differs"
+    assert np.abs(of - o_ref).max() <= O_TOL
+    assert np.abs(lf[fin] - lse_ref[fin]).max() <= LSE_TOL
+
+
+def test_single_token_reproduces_fa_decode_splitkv(fa):
+    dev = torch.device("cuda:0")
+    q, kc, vc, lens = (t.to(dev) for t in inputs.make_decode(3, 16, 4, 128, 3000, 1, 3000, seed=5))
+    o1, l1 = fa.fa_decode_splitkv(q, kc, vc, lens, num_splits=6)
+    o2, l2 = fa.fa_decode_splitkv_multi(q, kc, vc, lens, causal=True, num_splits=6)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2[:, :, 0])
+
+
+def test_multi_token_full_size(fa):
+    """The decode workload with 4 speculative tokens per sequence (B=8, Hq=32, Hkv=8,
+    so 4 heads x 4 tokens = 16 columns), causal; every output against the oracle."""
+    w = inputs.DECODE
+    q1, kc, vc, lens = inputs.decode_inputs(w)
+    g = torch.Generator().manual_seed(12)
+    q = torch.randn((w.B, 4, w.Hq, w.D), generator=g).to(torch.bfloat16)
+    dev = torch.device("cuda:0")
+    o, lse = fa.fa_decode_splitkv_multi(q.to(dev), kc.to(dev), vc.to(dev), lens.to(dev), causal=True)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.decode_multi(q, kc, vc, lens.numpy(), scale=w.scale, causal=True)
+    assert np.abs(o.float().cpu().numpy() - o_ref).max() <= O_TOL
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_TOL
+
+
+def test_multi_rejects_too_many_columns(fa):
+    dev = torch.device("cuda:0")
+    q, kc, vc, lens = (t.to(dev) for t in _make(1, 5, 8, 2, 128, 256, [100], seed=1))
+    with pytest.raises(fa.FaError) as e:
+        fa.fa_decode_splitkv_multi(q, kc, vc, lens)  # 4 heads x 5 tokens = 20 > 16
+    assert e.value.status == 2

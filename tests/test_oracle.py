@@ -436,3 +436,29 @@ def test_varlen_sequences_are_independent_and_empty_ones_are_zero():
     k2[5:] += 3.0  # other sequences' keys do not touch sequence 0
     o2, _ = oracle.fwd_varlen(q, k2, v, cq, ck, scale=0.7)
     assert np.array_equal(o2[0:4], o[0:4])
+
+
+def test_decode_multi_reduces_to_single_token_decode():
+    q, kc, vc, lens = _decode_case()
+    o1, l1 = oracle.decode(q, kc, vc, lens, scale=0.3)
+    o2, l2 = oracle.decode_multi(q, kc, vc, lens, scale=0.3, causal=True)
+    assert np.array_equal(o2[:, 0], o1) and np.array_equal(l2[:, :, 0], l1)
+
+
+def test_decode_multi_causal_rows_see_growing_prefixes():
+    """Query s of sequence b sees keys [0, len - Sq + s]: with Q = 0 its output is the
+    mean of exactly those V rows."""
+    rng = np.random.default_rng(4)
+    B, Sq, Hq, Hkv, D, smax = 2, 3, 2, 1, 8, 10
+    q = np.zeros((B, Sq, Hq, D))
+    kc, vc = rng.standard_normal((B, smax, Hkv, D)), rng.standard_normal((B, smax, Hkv, D))
+    lens = [7, 2]
+    o, lse = oracle.decode_multi(q, kc, vc, lens, scale=1.0, causal=True)
+    for b in range(B):
+        for s in range(Sq):
+            n = lens[b] - Sq + s + 1
+            if n <= 0:
+                assert np.all(o[b, s] == 0) and np.all(lse[b, :, s] == -np.inf)
+            else:
+                assert np.allclose(o[b, s, 0], vc[b, :n, 0].mean(0), atol=1e-14)
+                assert lse[b, 0, s] == pytest.approx(math.log(n), abs=1e-14)
