@@ -50,6 +50,9 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", action="store_true",
+                    help="instead of the step, time each widened entry point (window, varlen, "
+                         "paged and multi-token decode) and print one JSON line per row")
     return ap.parse_args(argv)
 
 
@@ -461,9 +464,119 @@ def run_reference(args, rank, world):
     print(json.dumps(out), flush=True)
 
 
+# ----------------------------------------------------------- widened rows ----
+
+def _time_ms(fn, reps=10, warmup=3):
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_rows(args):
+    """One JSON line per widened entry point, each with its roofline.  Forward variants
+    count the visible (query, key) pairs: 4 * D * pairs * Hq FLOPs; decode variants count
+    the valid K/V bytes plus Q, O and LSE."""
+    import numpy as np
+    import torch
+
+    import exact_tiled_attention_20_gb300 as fa
+    from exact_tiled_attention_20_gb300 import build, inputs
+
+    build.build_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peaks, src = load_peaks()
+    peak_t = float(peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"])
+    peak_h = float(peaks["hbm_gbs"])
+
+    def emit(row, workload, ms, achieved, unit, bound, extra=None):
+        peak = peak_t if bound == "tensor" else peak_h
+        d = {"row": row, "workload": workload, "ms": round(ms, 4), "value": round(achieved, 1),
+             "unit": unit, "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": peak,
+                                        "peak_source": f"{src}", "frac": round(achieved / peak, 4)}}
+        if extra:
+            d.update(extra)
+        print(json.dumps(d), flush=True)
+        if fa.fa_last_device_status() != 0:
+            raise RuntimeError(f"device status after {row}")
+
+    # sliding window: [16, 8192, 32, 128] causal, window of 1024 keys
+    w = inputs.PREFILL_LONG[0]
+    q, k, v = (t.to(dev) for t in inputs.fwd_inputs(w))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.Hq, w.Sq), device=dev)
+    win = 1023
+    ms = _time_ms(lambda: fa.fa_fwd(q, k, v, causal=True, window=(win, 0), out=o, lse=lse))
+    pairs = sum(min(i + 1, win + 1) for i in range(w.Sq))
+    flops = 4.0 * w.D * pairs * w.Hq * w.B
+    emit("sliding_window", "fa_fwd_window [16,8192,32,128] causal, window (1023, 0)", ms,
+         flops / ms / 1e9, "TFLOP/s", "tensor")
+    # variable length: 16 sequences of U[256, 8192] rows, causal, packed
+    rng = np.random.default_rng(1005)
+    lens = [int(x) for x in rng.integers(256, 8193, 16)]
+    tq = sum(lens)
+    qv, kv_, vv = q.view(-1, w.Hq, w.D)[:tq], k.view(-1, w.Hkv, w.D)[:tq], v.view(-1, w.Hkv, w.D)[:tq]
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device=dev)
+    ov = torch.empty_like(qv)
+    lv = torch.empty((w.Hq, tq), device=dev)
+    ms = _time_ms(lambda: fa.fa_fwd_varlen(qv, kv_, vv, cu, cu, causal=True, out=ov, lse=lv))
+    pairs = sum(n * (n + 1) // 2 for n in lens)
+    emit("varlen", f"fa_fwd_varlen 16 sequences U[256,8192] (total {tq}), Hq=Hkv=32, D=128, causal",
+         ms, 4.0 * w.D * pairs * w.Hq / ms / 1e9, "TFLOP/s", "tensor")
+    del q, k, v, o, lse, qv, kv_, vv, ov, lv
+    torch.cuda.empty_cache()
+    # decode variants on the decode workload
+    wd = inputs.DECODE
+    dq, dk, dv, dl = inputs.decode_inputs(wd)
+    nbytes = decode_bytes(wd, dl.tolist())
+    page = 256
+    mp = wd.Smax // page
+    perm = torch.randperm(wd.B * mp, generator=torch.Generator().manual_seed(7))
+    table = perm.view(wd.B, mp).to(torch.int32)
+    kp = torch.empty((wd.B * mp, page, wd.Hkv, wd.D), dtype=dk.dtype)
+    vp = torch.empty_like(kp)
+    kp[perm] = dk.view(wd.B * mp, page, wd.Hkv, wd.D)
+    vp[perm] = dv.view(wd.B * mp, page, wd.Hkv, wd.D)
+    dqd, kpd, vpd, tbd, dld = (t.to(dev) for t in (dq, kp, vp, table, dl))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flushed(fn):
+        def run():
+            flush.sum()  # read 256 MiB to evict the cache from L2 (clean lines)
+            fn()
+        return run
+    base = _time_ms(flushed(lambda: None))
+    ms = _time_ms(flushed(lambda: fa.fa_decode_splitkv_paged(dqd, kpd, vpd, tbd, dld))) - base
+    emit("paged_decode", "fa_decode_splitkv_paged, decode workload in 256-key pages (random page order)",
+         ms, nbytes / ms / 1e6, "GB/s", "hbm")
+    del kpd, vpd
+    dkd, dvd = dk.to(dev), dv.to(dev)
+    ms = _time_ms(flushed(lambda: fa.fa_decode_splitkv(dqd, dkd, dvd, dld))) - base
+    emit("decode", "fa_decode_splitkv, decode workload (L2 flushed by a 256 MiB read between calls)",
+         ms, nbytes / ms / 1e6, "GB/s", "hbm")
+    q4 = torch.randn((wd.B, 4, wd.Hq, wd.D), device=dev).to(torch.bfloat16)
+    nb4 = nbytes + 3 * wd.B * wd.Hq * wd.D * 2 * 2
+    ms = _time_ms(flushed(lambda: fa.fa_decode_splitkv_multi(q4, dkd, dvd, dld, causal=True))) - base
+    emit("multi_token_decode", "fa_decode_splitkv_multi, decode workload with 4 causal tokens",
+         ms, nb4 / ms / 1e6, "GB/s", "hbm")
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, local_rank, world = dist_env()
+    if args.rows:
+        if rank == 0:
+            run_rows(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
         return

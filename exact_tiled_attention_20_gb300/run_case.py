@@ -3,6 +3,7 @@ profiling a single kernel (e.g. under ncu) on inputs resident on the GPU.
 
   python -m exact_tiled_attention_20_gb300.run_case fwd B S Hq Hkv D causal [iters]
   python -m exact_tiled_attention_20_gb300.run_case decode B Hq Hkv D Smax [iters]
+  python -m exact_tiled_attention_20_gb300.run_case decode_workload [iters]
 
 Inputs are drawn on the device from a fixed seed (values do not matter for profiling);
 the script prints the mean time per call from CUDA events.
@@ -41,6 +42,17 @@ def main(argv):
         lens = torch.randint(Smax // 32, Smax + 1, (B,), device=dev, generator=g, dtype=torch.int32)
         ns = fa.fa_decode_default_splits(B, Hkv, Smax)
         ws = torch.empty(fa.fa_decode_workspace_bytes(B, Hq, D, ns), dtype=torch.uint8, device=dev)
+        o = torch.empty_like(q)
+        call = lambda: fa.fa_decode_splitkv(q, kc, vc, lens, num_splits=ns, workspace=ws, out=o)  # noqa: E731
+    elif kind == "decode_workload":
+        # the benchmark's decode workload, same seeded inputs and default split count
+        from . import inputs
+
+        w = inputs.DECODE
+        iters = int(argv[1]) if len(argv) > 1 else 3
+        q, kc, vc, lens = (t.to(dev) for t in inputs.decode_inputs(w))
+        ns = fa.fa_decode_default_splits(w.B, w.Hkv, w.Smax)
+        ws = torch.empty(fa.fa_decode_workspace_bytes(w.B, w.Hq, w.D, ns), dtype=torch.uint8, device=dev)
         o = torch.empty_like(q)
         call = lambda: fa.fa_decode_splitkv(q, kc, vc, lens, num_splits=ns, workspace=ws, out=o)  # noqa: E731
     else:
