@@ -84,6 +84,10 @@ struct FwdConfig {
     // O-done is signalled after every P.V when S is issued ahead of P.V (NQ == 1), and
     // only after a tile's last P.V otherwise.
     static constexpr bool kOPerIter = (NQ == 1);
+    // With two Q tiles the K/V ring stages are released by the second softmax warpgroup:
+    // S1(j) completing implies S0(j) and every earlier P.V completed, so K_j and V_{j-1}
+    // are free.  That saves the tensor pipe two tcgen05.commit per iteration.
+    static constexpr bool kRingBySoftmax = (NQ > 1);
     static constexpr int kProducerWarp = 4 * NQ;
     static constexpr int kMmaWarp = 4 * NQ + 1;
     // barrier indices
@@ -334,14 +338,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 if (!ok) break;
                 {
                     const uint32_t st = kv_it % C::NS;
+                    // TMA-filled operands need no tcgen05 fence: the mbarrier wait orders them.
                     ok = mbar_wait(bar(C::kBarKFull + st), (kv_it / C::NS) & 1u, wc);
                     if (!ok) break;
-                    tc_fence_after();
                     for (int q = 0; q < C::NQ; ++q) {
                         issue_s(q, st, slot_of(q, it));
                         umma_commit(bar(C::kBarSFull + slot_of(q, it)));
                     }
-                    umma_commit(bar(C::kBarKEmpty + st));
+                    if (!C::kRingBySoftmax) umma_commit(bar(C::kBarKEmpty + st));
                     if (n == 1)
                         for (int q = 0; q < C::NQ; ++q) umma_commit(bar(C::kBarQEmpty + q));
                 }
@@ -373,16 +377,16 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                             if (q == 0) {
                                 ok = mbar_wait(bar(C::kBarKFull + nst), ((cur + 1) / C::NS) & 1u, wc);
                                 if (!ok) break;
-                                tc_fence_after();
                             }
                             issue_s(q, nst, slot_of(q, it + 1));
                             umma_commit(bar(C::kBarSFull + slot_of(q, it + 1)));
-                            if (q == C::NQ - 1) umma_commit(bar(C::kBarKEmpty + nst));
+                            if (!C::kRingBySoftmax && q == C::NQ - 1)
+                                umma_commit(bar(C::kBarKEmpty + nst));
                             if (j + 2 == n) umma_commit(bar(C::kBarQEmpty + q));
                         }
                     }
                     if (!ok) break;
-                    umma_commit(bar(C::kBarVEmpty + st));
+                    if (!C::kRingBySoftmax) umma_commit(bar(C::kBarVEmpty + st));
                     ++it;
                 }
                 kv_it += n;
@@ -434,6 +438,10 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 ok = mbar_wait(bar(C::kBarSFull + slot), spar, wc);
                 if (!ok) break;
                 tc_fence_after();
+                if (C::kRingBySoftmax && q == C::NQ - 1 && wq == 0 && lane == 0) {
+                    mbar_arrive(bar(C::kBarKEmpty + it % C::NS));  // K of this block
+                    if (it > 0) mbar_arrive(bar(C::kBarVEmpty + (it - 1) % C::NS));  // V of the last
+                }
                 const uint32_t tS = lane_base + slot * C::BN;
                 // All chunks of S are loaded before a single wait.
                 uint32_t u[kSC][32];
