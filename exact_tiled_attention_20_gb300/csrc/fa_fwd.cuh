@@ -291,40 +291,50 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         __syncwarp();
     } else if (warp == C::kMmaWarp) {
         // ------------------------------------------------------------- MMA issuer ----
-        if (lane == 0) {
+        // The whole warp runs this loop and one elected lane issues each tcgen05.mma and
+        // tcgen05.commit: uniform control flow keeps the issue cheap, and the issue rate
+        // is what feeds the tensor pipe.  Every lane waits on the barriers itself and the
+        // outcome is voted, so the warp stays converged (elect.sync needs all 32 lanes)
+        // even when a wait gives up.
+        {
             constexpr uint32_t idesc_s = make_idesc_f16(128, C::BN, kBF16, false, false);
             constexpr uint32_t idesc_o = make_idesc_f16(128, C::D, kBF16, false, true);
             uint32_t kv_it = 0, tcount = 0, it = 0;
             bool ok = true;
+            auto wait = [&](uint32_t b, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait(b, parity, wc));
+            };
 
             // Descriptors are built once; stepping K by 16 elements only advances the
-            // start-address field, so each MMA issues with a constant 64-bit add.  The
-            // issuing thread is on the critical path: keep this loop lean.
-            const uint64_t dq0 = make_sdesc_sw128(sQ, 16, 1024);
-            const uint64_t dk0 = make_sdesc_sw128(sK, 16, 1024);
-            const uint64_t dv0 = make_sdesc_sw128(sV, C::BN * 128, 1024);
+            // start-address field in the low word, so each MMA issues with a constant
+            // 32-bit add.
+            const uint64_t dq = make_sdesc_sw128(sQ, 16, 1024);
+            const uint64_t dk = make_sdesc_sw128(sK, 16, 1024);
+            const uint64_t dv = make_sdesc_sw128(sV, C::BN * 128, 1024);
+            const uint32_t q_lo = (uint32_t)dq, q_hi = (uint32_t)(dq >> 32);
+            const uint32_t k_lo = (uint32_t)dk, k_hi = (uint32_t)(dk >> 32);
+            const uint32_t v_lo = (uint32_t)dv, v_hi = (uint32_t)(dv >> 32);
             auto issue_s = [&](int q, uint32_t kst, uint32_t slot) {
                 const uint32_t d = tmem + slot * C::BN;
-                const uint64_t a = dq0 + (uint64_t)((q * C::kQBytes) >> 4);
-                const uint64_t b = dk0 + (uint64_t)((kst * C::kKVBytes) >> 4);
-                umma_ss_imm<false>(d, a, b, idesc_s);
+                const uint32_t a = q_lo + (uint32_t)((q * C::kQBytes) >> 4);
+                const uint32_t b = k_lo + ((kst * C::kKVBytes) >> 4);
+                umma_ss_elect<false>(d, a, q_hi, b, k_hi, idesc_s);
 #pragma unroll
                 for (int kk = 1; kk < C::D / 16; ++kk)
-                    umma_ss_imm<true>(d, a + (uint64_t)(((kk >> 2) * (C::BM * 128) + (kk & 3) * 32) >> 4),
-                                      b + (uint64_t)(((kk >> 2) * (C::BN * 128) + (kk & 3) * 32) >> 4),
-                                      idesc_s);
+                    umma_ss_elect<true>(d, a + (((kk >> 2) * (C::BM * 128) + (kk & 3) * 32) >> 4), q_hi,
+                                        b + (((kk >> 2) * (C::BN * 128) + (kk & 3) * 32) >> 4), k_hi, idesc_s);
             };
             auto issue_pv = [&](int q, uint32_t vst, uint32_t slot, bool acc) {
                 const uint32_t d = tmem + C::kOCol0 + q * C::D;
                 const uint32_t a = tmem + slot * C::BN;
-                const uint64_t b = dv0 + (uint64_t)((vst * C::kKVBytes) >> 4);
+                const uint32_t b = v_lo + ((vst * C::kKVBytes) >> 4);
                 if (acc)
-                    umma_ts_imm<true>(d, a, b, idesc_o);
+                    umma_ts_elect<true>(d, a, b, v_hi, idesc_o);
                 else
-                    umma_ts_imm<false>(d, a, b, idesc_o);
+                    umma_ts_elect<false>(d, a, b, v_hi, idesc_o);
 #pragma unroll
                 for (int kk = 1; kk < C::BN / 16; ++kk)
-                    umma_ts_imm<true>(d, a + kk * 8, b + (uint64_t)((kk * (16 * 128)) >> 4), idesc_o);
+                    umma_ts_elect<true>(d, a + kk * 8, b + ((kk * (16 * 128)) >> 4), v_hi, idesc_o);
             };
             auto slot_of = [&](int q, uint32_t iter) -> uint32_t {
                 return C::NQ == 1 ? (iter & 1u) : (uint32_t)q;
@@ -334,20 +344,20 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 const TileCoord c = decode_tile<C>(p, vtab, t);
                 const int n = c.n_kv;
                 if (n == 0) continue;
-                for (int q = 0; q < C::NQ && ok; ++q) ok = mbar_wait(bar(C::kBarQFull + q), tcount & 1u, wc);
+                for (int q = 0; q < C::NQ && ok; ++q) ok = wait(bar(C::kBarQFull + q), tcount & 1u);
                 if (!ok) break;
                 {
                     const uint32_t st = kv_it % C::NS;
                     // TMA-filled operands need no tcgen05 fence: the mbarrier wait orders them.
-                    ok = mbar_wait(bar(C::kBarKFull + st), (kv_it / C::NS) & 1u, wc);
+                    ok = wait(bar(C::kBarKFull + st), (kv_it / C::NS) & 1u);
                     if (!ok) break;
                     for (int q = 0; q < C::NQ; ++q) {
                         issue_s(q, st, slot_of(q, it));
-                        umma_commit(bar(C::kBarSFull + slot_of(q, it)));
+                        umma_commit_elect(bar(C::kBarSFull + slot_of(q, it)));
                     }
-                    if (!C::kRingBySoftmax) umma_commit(bar(C::kBarKEmpty + st));
+                    if (!C::kRingBySoftmax) umma_commit_elect(bar(C::kBarKEmpty + st));
                     if (n == 1)
-                        for (int q = 0; q < C::NQ; ++q) umma_commit(bar(C::kBarQEmpty + q));
+                        for (int q = 0; q < C::NQ; ++q) umma_commit_elect(bar(C::kBarQEmpty + q));
                 }
                 for (int j = 0; j < n && ok; ++j) {
                     const uint32_t cur = kv_it + j;
@@ -355,48 +365,48 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     const uint32_t nst = (cur + 1) % C::NS;
                     const bool more = (j + 1 < n);
                     if (C::NQ == 1 && more) {
-                        ok = mbar_wait(bar(C::kBarKFull + nst), ((cur + 1) / C::NS) & 1u, wc);
+                        ok = wait(bar(C::kBarKFull + nst), ((cur + 1) / C::NS) & 1u);
                         if (!ok) break;
                         tc_fence_after();
                         issue_s(0, nst, slot_of(0, it + 1));
-                        umma_commit(bar(C::kBarSFull + slot_of(0, it + 1)));
-                        umma_commit(bar(C::kBarKEmpty + nst));
-                        if (j + 2 == n) umma_commit(bar(C::kBarQEmpty + 0));
+                        umma_commit_elect(bar(C::kBarSFull + slot_of(0, it + 1)));
+                        umma_commit_elect(bar(C::kBarKEmpty + nst));
+                        if (j + 2 == n) umma_commit_elect(bar(C::kBarQEmpty + 0));
                     }
-                    ok = mbar_wait(bar(C::kBarVFull + st), (cur / C::NS) & 1u, wc);
+                    ok = wait(bar(C::kBarVFull + st), (cur / C::NS) & 1u);
                     if (!ok) break;
                     for (int q = 0; q < C::NQ && ok; ++q) {
-                        ok = mbar_wait(bar(C::kBarPFull + q), it & 1u, wc);
+                        ok = wait(bar(C::kBarPFull + q), it & 1u);
                         if (ok && j == 0 && tcount > 0)
-                            ok = mbar_wait(bar(C::kBarODrained + q), (tcount - 1) & 1u, wc);
+                            ok = wait(bar(C::kBarODrained + q), (tcount - 1) & 1u);
                         if (!ok) break;
                         tc_fence_after();
                         issue_pv(q, st, slot_of(q, it), j > 0);
-                        if (kOPerIter || j + 1 == n) umma_commit(bar(C::kBarODone + q));
+                        if (kOPerIter || j + 1 == n) umma_commit_elect(bar(C::kBarODone + q));
                         if (C::NQ > 1 && more) {
                             if (q == 0) {
-                                ok = mbar_wait(bar(C::kBarKFull + nst), ((cur + 1) / C::NS) & 1u, wc);
+                                ok = wait(bar(C::kBarKFull + nst), ((cur + 1) / C::NS) & 1u);
                                 if (!ok) break;
                             }
                             issue_s(q, nst, slot_of(q, it + 1));
-                            umma_commit(bar(C::kBarSFull + slot_of(q, it + 1)));
+                            umma_commit_elect(bar(C::kBarSFull + slot_of(q, it + 1)));
                             if (!C::kRingBySoftmax && q == C::NQ - 1)
-                                umma_commit(bar(C::kBarKEmpty + nst));
-                            if (j + 2 == n) umma_commit(bar(C::kBarQEmpty + q));
+                                umma_commit_elect(bar(C::kBarKEmpty + nst));
+                            if (j + 2 == n) umma_commit_elect(bar(C::kBarQEmpty + q));
                         }
                     }
                     if (!ok) break;
-                    if (!C::kRingBySoftmax) umma_commit(bar(C::kBarVEmpty + st));
+                    if (!C::kRingBySoftmax) umma_commit_elect(bar(C::kBarVEmpty + st));
                     ++it;
                 }
                 kv_it += n;
                 ++tcount;
             }
             // Every MMA issued has completed before TMEM and shared memory are released.
-            umma_commit(bar(C::kBarFinal));
+            umma_commit_elect(bar(C::kBarFinal));
             mbar_wait_drain(bar(C::kBarFinal), 0);
+            __syncwarp();
         }
-        __syncwarp();
     } else {
         // ------------------------------------------------------ softmax warpgroups ----
         const int q = warp >> 2;
