@@ -554,11 +554,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             f2_unpack(l2, l0, l1);
             const float l_run = l0 + l1;
             const float inv_l = (l_run > 0.f) ? 1.0f / l_run : 0.f;
-#pragma unroll
-            for (int ch = 0; ch < C::D / 32; ++ch) {
-                uint32_t ov[32];
-                tmem_ld_32x32b_x32(tO + ch * 32, ov);
-                tmem_wait_ld(ov);
+            auto store_chunk = [&](int ch, const uint32_t (&ov)[32]) {
                 uint32_t w[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
@@ -570,10 +566,34 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                         st_global_v4(orow + ch * 32 + v4 * 8, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
                                      w[4 * v4 + 3]);
                 }
+            };
+            if constexpr (C::D <= 128) {
+                // All of O comes out of TMEM behind one wait and the accumulator is handed
+                // back before the normalisation and the global stores, so the next tile's
+                // first P.V does not wait for them.
+                uint32_t ov[C::D / 32][32];
+#pragma unroll
+                for (int ch = 0; ch < C::D / 32; ++ch) tmem_ld_32x32b_x32(tO + ch * 32, ov[ch]);
+                tmem_wait_ld(ov[0]);
+#pragma unroll
+                for (int ch = 1; ch < C::D / 32; ++ch) reg_fence(ov[ch]);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::kBarODrained + q));
+#pragma unroll
+                for (int ch = 0; ch < C::D / 32; ++ch) store_chunk(ch, ov[ch]);
+            } else {
+#pragma unroll
+                for (int ch = 0; ch < C::D / 32; ++ch) {
+                    uint32_t ov[32];
+                    tmem_ld_32x32b_x32(tO + ch * 32, ov);
+                    tmem_wait_ld(ov);
+                    store_chunk(ch, ov);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::kBarODrained + q));
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::kBarODrained + q));
             if (p.lse && row_ok) {
                 const float lse = (l_run > 0.f) ? (m_run + lg2_approx(l_run)) * 0.69314718055994531f
                                                 : kNegInf;
