@@ -248,6 +248,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (lane == 0) {
             uint32_t kv_it = 0, icount = 0;
             bool ok = true;
+            // Every K/V row is read exactly once by this kernel.
+            const uint64_t kv_policy = l2_policy_evict_first();
             for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
                 const DecItem it = decode_item(T, p.B, p.Hkv, idx);
                 const uint32_t qs = icount & 1u;
@@ -276,8 +278,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(kDBarKFull + st), kDecKVBytes);
                     for (int a = 0; a < kDecDA; ++a)
-                        tma_load_4d(sK + st * kDecKVBytes + a * (kDecBN * 128), &tm_k,
-                                    bar(kDBarKFull + st), a * 64, it.hk, c2, c3);
+                        tma_load_4d_hint(sK + st * kDecKVBytes + a * (kDecBN * 128), &tm_k,
+                                         bar(kDBarKFull + st), a * 64, it.hk, c2, c3, kv_policy);
                     ok = mbar_wait(bar(kDBarVEmpty + st), ph, wc);
                     if (!ok) {
                         mbar_wait_drain(bar(kDBarKFull + st), (kv_it / kDecNS) & 1u);
@@ -285,8 +287,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     }
                     mbar_arrive_expect_tx(bar(kDBarVFull + st), kDecKVBytes);
                     for (int a = 0; a < kDecDA; ++a)
-                        tma_load_4d(sV + st * kDecKVBytes + a * (kDecBN * 128), &tm_v,
-                                    bar(kDBarVFull + st), a * 64, it.hk, c2, c3);
+                        tma_load_4d_hint(sV + st * kDecKVBytes + a * (kDecBN * 128), &tm_v,
+                                         bar(kDBarVFull + st), a * 64, it.hk, c2, c3, kv_policy);
                     ++kv_it;
                 }
                 ++icount;
