@@ -76,15 +76,15 @@ constexpr int kDBarVFull = kDBarKEmpty + kDecNS;
 constexpr int kDBarVEmpty = kDBarVFull + kDecNS;
 constexpr int kDBarSFull = kDBarVEmpty + kDecNS;  // 2
 constexpr int kDBarPFull = kDBarSFull + 2;
-constexpr int kDBarODone = kDBarPFull + 1;
-constexpr int kDBarODrained = kDBarODone + 1;
+constexpr int kDBarODone = kDBarPFull + 1;       // 2: one per P^T buffer
+constexpr int kDBarODrained = kDBarODone + 2;
 constexpr int kDBarFinal = kDBarODrained + 1;
 constexpr int kDNumBars = kDBarFinal + 1;
 
 struct DecSmemTail {
     uint64_t bars[kDNumBars];
-    float red[2][4][16];   // per-tile cross-warp max, double-buffered
-    float lred[4][16];     // end-of-item cross-warp sums
+    alignas(16) float red[2][4][16];   // per-tile cross-warp max, double-buffered
+    alignas(16) float lred[4][16];     // end-of-item cross-warp sums
     int lens[kDecMaxB];
     int prefix[kDecMaxB + 1];  // exclusive prefix of n_b * Hkv
     int warp_sums[4];
@@ -95,7 +95,9 @@ struct DecSmemTail {
     int abort_flag;
 };
 
-constexpr int kDecTileBytes = 2 * kDecNS * kDecKVBytes + 2 * kDecQBytes + kDecPBytes;
+// P^T is double-buffered: the compute warps write tile j's while P.V of tile j-1 reads
+// the other buffer.
+constexpr int kDecTileBytes = 2 * kDecNS * kDecKVBytes + 2 * kDecQBytes + 2 * kDecPBytes;
 constexpr int kDecSmemBytes = 1024 + kDecTileBytes + (int)sizeof(DecSmemTail);
 static_assert(kDecSmemBytes <= 232448, "decode shared memory budget");
 
@@ -139,6 +141,43 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Per-column reduction over the 32 lanes of a warp for N = 4, 8 or 16 columns: each of
+// the first log2(N) butterfly steps halves the columns a lane carries (it keeps one half
+// and trades the other with its partner), the remaining steps combine plain values.
+// Afterwards lane l holds the result for column reduce_col<N>(l).  N - 1 + 5 - log2(N)
+// shuffles instead of 5 N.
+template <int N>
+__device__ __forceinline__ int reduce_col(int lane) {
+    int col = 0, n = N, m = 16;
+#pragma unroll
+    for (; n > 1; n >>= 1, m >>= 1)
+        if (lane & m) col += n / 2;
+    return col;
+}
+
+template <int N, bool kMax>
+__device__ __forceinline__ float warp_reduce_cols(float (&v)[N], int lane) {
+    int m = 16;
+#pragma unroll
+    for (int n = N; n > 1; n >>= 1, m >>= 1) {
+        const bool up = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float send = up ? v[i] : v[i + n / 2];
+            const float keep = up ? v[i + n / 2] : v[i];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, m);
+            v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (; m > 0; m >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, r, m);
+        r = kMax ? fmaxf(r, o) : r + o;
+    }
+    return r;
 }
 
 template <bool kBF16>
@@ -186,7 +225,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         prefetch_tmap(&tm_v);
     }
     // P^T rows past the group stay zero for the whole kernel.
-    for (int i = tid; i < kDecPBytes / 4; i += kDecThreads)
+    for (int i = tid; i < 2 * kDecPBytes / 4; i += kDecThreads)
         reinterpret_cast<uint32_t*>(base_gen + (sP - base))[i] = 0u;
     fence_proxy_async_smem();
     __syncthreads();
@@ -325,16 +364,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     umma_ss_imm<true>(d, a + (uint64_t)(((kk >> 2) * (kDecBN * 128) + (kk & 3) * 32) >> 4),
                                       b + (uint64_t)(((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), idesc_s);
             };
-            auto issue_pv = [&](uint32_t vst, bool acc) {
+            auto issue_pv = [&](uint32_t vst, uint32_t pbuf, bool acc) {
                 const uint64_t a = dv0 + (uint64_t)((vst * kDecKVBytes) >> 4);
+                const uint64_t b = dp0 + (uint64_t)((pbuf * kDecPBytes) >> 4);
                 if (acc)
-                    umma_ss_imm<true>(tmem + 32, a, dp0, idesc_o);
+                    umma_ss_imm<true>(tmem + 32, a, b, idesc_o);
                 else
-                    umma_ss_imm<false>(tmem + 32, a, dp0, idesc_o);
+                    umma_ss_imm<false>(tmem + 32, a, b, idesc_o);
 #pragma unroll
                 for (int kk = 1; kk < kDecBN / 16; ++kk)
                     umma_ss_imm<true>(tmem + 32, a + (uint64_t)((kk * (16 * 128)) >> 4),
-                                      dp0 + (uint64_t)(((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), idesc_o);
+                                      b + (uint64_t)(((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), idesc_o);
             };
             for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
                 const DecItem item = decode_item(T, p.B, p.Hkv, idx);
@@ -371,8 +411,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     if (ok) ok = mbar_wait(bar(kDBarVFull + st), (cur / kDecNS) & 1u, wc);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_pv(st, j > 0);
-                    umma_commit(bar(kDBarODone));
+                    issue_pv(st, it_s & 1u, j > 0);
+                    umma_commit(bar(kDBarODone + (it_s & 1u)));
                     umma_commit(bar(kDBarVEmpty + st));
                     ++it_s;
                 }
@@ -410,24 +450,33 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 const bool valid = key < item.k1;
                 const int ncols = g * p.sq;
                 const int lim0 = T.lens[item.b] - p.sq;  // token s sees keys <= lim0 + s
-                float sv[GMAX];
+                float sv[GMAX], mx[GMAX];
 #pragma unroll
                 for (int h = 0; h < GMAX; ++h) {
                     const bool vis = valid && h < ncols && (!p.causal || key <= lim0 + h / g);
                     sv[h] = vis ? __uint_as_float(u[h]) : kNegInf;
-                    float m = sv[h];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                    if (lane == 0) T.red[j & 1][warp][h] = m;
+                    mx[h] = sv[h];
                 }
+                // per-column max over this warp's 32 keys, then over the four warps
+                const float wm = warp_reduce_cols<GMAX, true>(mx, lane);
+                if ((lane & (32 / GMAX - 1)) == 0) T.red[j & 1][warp][reduce_col<GMAX>(lane)] = wm;
                 named_bar_sync(1, 128);
+                float mb4[GMAX];
+#pragma unroll
+                for (int h4 = 0; h4 < GMAX; h4 += 4) {
+                    float4 r[4];
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) r[w] = *reinterpret_cast<const float4*>(&T.red[j & 1][w][h4]);
+                    mb4[h4 + 0] = fmaxf(fmaxf(r[0].x, r[1].x), fmaxf(r[2].x, r[3].x));
+                    mb4[h4 + 1] = fmaxf(fmaxf(r[0].y, r[1].y), fmaxf(r[2].y, r[3].y));
+                    mb4[h4 + 2] = fmaxf(fmaxf(r[0].z, r[1].z), fmaxf(r[2].z, r[3].z));
+                    mb4[h4 + 3] = fmaxf(fmaxf(r[0].w, r[1].w), fmaxf(r[2].w, r[3].w));
+                }
                 float alpha[GMAX], msub[GMAX];
                 bool any_rescale = false;
 #pragma unroll
                 for (int h = 0; h < GMAX; ++h) {
-                    const float mb = fmaxf(fmaxf(T.red[j & 1][0][h], T.red[j & 1][1][h]),
-                                           fmaxf(T.red[j & 1][2][h], T.red[j & 1][3][h])) *
-                                     p.scale_log2;
+                    const float mb = mb4[h] * p.scale_log2;
                     const bool bump = mb > m_run[h] + 8.0f;
                     const float mn = bump ? mb : m_run[h];
                     alpha[h] = bump ? ex2_approx(m_run[h] - mn) : 1.0f;
@@ -441,23 +490,27 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     pv[h] = ex2_approx(fmaf(sv[h], p.scale_log2, -msub[h]));
                     l_part[h] = l_part[h] * alpha[h] + pv[h];
                 }
-                if (j > 0) {
-                    // the previous P.V has finished reading P^T and may now be rescaled
-                    ok = mbar_wait(bar(kDBarODone), (it_s - 1) & 1u, wc);
+                // This tile's P^T buffer was last read by the P.V of tile it_s - 2.
+                if (it_s >= 2) {
+                    ok = mbar_wait(bar(kDBarODone + (it_s & 1u)), ((it_s - 2) >> 1) & 1u, wc);
+                    if (!ok) break;
+                }
+                if (j > 0 && any_rescale) {  // uniform: every thread saw the same maxima
+                    // the previous P.V must have finished accumulating into O
+                    ok = mbar_wait(bar(kDBarODone + ((it_s - 1) & 1u)), ((it_s - 1) >> 1) & 1u, wc);
                     if (!ok) break;
                     tc_fence_after();
-                    if (any_rescale) {  // uniform: every thread saw the same maxima
-                        uint32_t ov[16];
-                        tmem_ld_32x32b_x16(lane_base + 32, ov);
-                        tmem_wait_ld(ov);
+                    uint32_t ov[16];
+                    tmem_ld_32x32b_x16(lane_base + 32, ov);
+                    tmem_wait_ld(ov);
 #pragma unroll
-                        for (int h = 0; h < GMAX; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
-                        tmem_st_32x32b_x16(lane_base + 32, ov);
-                        tmem_wait_st();
-                    }
+                    for (int h = 0; h < GMAX; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
+                    tmem_st_32x32b_x16(lane_base + 32, ov);
+                    tmem_wait_st();
                 }
+                const uint32_t sPb = sP + (it_s & 1u) * kDecPBytes;
 #pragma unroll
-                for (int h = 0; h < GMAX; ++h) st_shared_u16(pt_addr(sP, h, tid), to16<kBF16>(pv[h]));
+                for (int h = 0; h < GMAX; ++h) st_shared_u16(pt_addr(sPb, h, tid), to16<kBF16>(pv[h]));
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(bar(kDBarPFull));
@@ -465,7 +518,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             }
             if (!ok) break;
             // ---- end of item: O^T / l -> partial output, log-sum-exp per head
-            ok = mbar_wait(bar(kDBarODone), (it_s - 1) & 1u, wc);
+            ok = mbar_wait(bar(kDBarODone + ((it_s - 1) & 1u)), ((it_s - 1) >> 1) & 1u, wc);
             if (!ok) break;
             tc_fence_after();
             uint32_t ov[16];
@@ -473,12 +526,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             tmem_wait_ld(ov);
             tc_fence_before();
             mbar_arrive(bar(kDBarODrained));
+            {
+                float ls[GMAX];
 #pragma unroll
-            for (int h = 0; h < GMAX; ++h) {
-                float s = l_part[h];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                if (lane == 0) T.lred[warp][h] = s;
+                for (int h = 0; h < GMAX; ++h) ls[h] = l_part[h];
+                const float wl = warp_reduce_cols<GMAX, false>(ls, lane);
+                if ((lane & (32 / GMAX - 1)) == 0) T.lred[warp][reduce_col<GMAX>(lane)] = wl;
             }
             named_bar_sync(1, 128);
 #pragma unroll
