@@ -75,8 +75,11 @@ constexpr int kDBarKEmpty = kDBarKFull + kDecNS;
 constexpr int kDBarVFull = kDBarKEmpty + kDecNS;
 constexpr int kDBarVEmpty = kDBarVFull + kDecNS;
 constexpr int kDBarSFull = kDBarVEmpty + kDecNS;  // 2
-constexpr int kDBarPFull = kDBarSFull + 2;
-constexpr int kDBarODone = kDBarPFull + 1;       // 2: one per P^T buffer
+// P full and O done: one barrier per P^T buffer.  With P^T double-buffered the compute
+// warps may finish tile j + 1 before the MMA warp has observed tile j; a single barrier
+// would then complete two phases ahead of its waiter and the parity wait would miss one.
+constexpr int kDBarPFull = kDBarSFull + 2;       // 2
+constexpr int kDBarODone = kDBarPFull + 2;       // 2
 constexpr int kDBarODrained = kDBarODone + 2;
 constexpr int kDBarFinal = kDBarODrained + 1;
 constexpr int kDNumBars = kDBarFinal + 1;
@@ -210,7 +213,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     // ---- setup: barriers, TMEM, and the work-item table from kv_lens
     if (tid == 0) {
         for (int i = 0; i < kDNumBars; ++i)
-            mbar_init(bar(i), (i == kDBarPFull || i == kDBarODrained) ? 128u : 1u);
+            mbar_init(bar(i), (i == kDBarPFull || i == kDBarPFull + 1 || i == kDBarODrained) ? 128u : 1u);
         T.abort_flag = 0;
         T.max_len = 0;
         fence_mbar_init();
@@ -405,7 +408,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                         umma_commit(bar(kDBarKEmpty + nst));
                         if (j + 2 == n) umma_commit(bar(kDBarQEmpty + qs));
                     }
-                    ok = mbar_wait(bar(kDBarPFull), it_s & 1u, wc);
+                    ok = mbar_wait(bar(kDBarPFull + (it_s & 1u)), (it_s >> 1) & 1u, wc);
                     if (ok && j == 0 && icount > 0)
                         ok = mbar_wait(bar(kDBarODrained), (icount - 1) & 1u, wc);
                     if (ok) ok = mbar_wait(bar(kDBarVFull + st), (cur / kDecNS) & 1u, wc);
@@ -447,13 +450,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 tmem_ld_32x32b_x16(lane_base + slot * 16, u);
                 tmem_wait_ld(u);
                 const int key = item.k0 + j * kDecBN + tid;
-                const bool valid = key < item.k1;
                 const int ncols = g * p.sq;
-                const int lim0 = T.lens[item.b] - p.sq;  // token s sees keys <= lim0 + s
+                // Token s sees keys <= len - sq + s; column h holds token h / g, so with
+                // causal tokens this key is visible to columns h >= (key - len + sq) * g.
+                const int lim0 = T.lens[item.b] - p.sq;
+                const int h_lo = p.causal ? max(key - lim0, 0) * g : 0;
+                const int h_hi = key < item.k1 ? ncols : 0;  // columns [h_lo, h_hi) see it
                 float sv[GMAX], mx[GMAX];
 #pragma unroll
                 for (int h = 0; h < GMAX; ++h) {
-                    const bool vis = valid && h < ncols && (!p.causal || key <= lim0 + h / g);
+                    const bool vis = h >= h_lo && h < h_hi;
                     sv[h] = vis ? __uint_as_float(u[h]) : kNegInf;
                     mx[h] = sv[h];
                 }
@@ -513,7 +519,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 for (int h = 0; h < GMAX; ++h) st_shared_u16(pt_addr(sPb, h, tid), to16<kBF16>(pv[h]));
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(bar(kDBarPFull));
+                mbar_arrive(bar(kDBarPFull + (it_s & 1u)));
                 ++it_s;
             }
             if (!ok) break;
