@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     for (int ch = 0; ch < kSC; ++ch)
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            if (ch * 32 + i > kmax || ch * 32 + i < kmin) u[ch][i] = 0xff800000u;  // -inf
+                            u[ch][i] = ((ch * 32 + i > kmax) | (ch * 32 + i < kmin)) ? 0xff800000u : u[ch][i];
                 }
                 // Row max over the BN scores: four independent chains of 3-input maxima.
                 auto sv = [&](int k) -> float { return __uint_as_float(u[k >> 5][k & 31]); };
