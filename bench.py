@@ -11,7 +11,8 @@ the whole step time; the decode's HBM GB/s is reported in the "decode" object.  
 are resident in HBM before the timed region and larger than L2 (4 GiB for the forward,
 1 GiB of KV cache for decode).  Each kernel is timed with CUDA events on the stream it is
 launched on.  `e2e` repeats the step through the public API from pinned host buffers,
-host<->device copies included.  `cpu_baseline` times the CPU oracle on a bounded sample
+every step's host<->device copies included, pipelined so that one step's compute overlaps
+the neighbouring steps' copies.  `cpu_baseline` times the CPU oracle on a bounded sample
 of the same workload on the host's cores.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -48,7 +49,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", action="store_true",
                     help="instead of the step, time each widened entry point (window, varlen, "
@@ -270,40 +271,73 @@ def run_native(args, rank, local_rank, world):
     dec_traffic = ncu_traffic("fa_decode_split_kernel")
 
     # ---- end to end through the public API, host buffers, copies inside the timed region
+    # Every step copies its inputs from pinned host memory, runs the step and reads its
+    # results back.  Steps are pipelined over two buffer sets on three streams (inputs in,
+    # compute, results out), so step i's compute overlaps step i+1's upload and step i-1's
+    # download; the timed region runs from the first upload to the last download.  (Spreading
+    # the uploads over several streams measured no faster: the host link is the limit.)
     e2e = None
     if args.e2e_steps > 0:
         pin = {n: t.pin_memory() for n, t in host.items()}
-        o_h = torch.empty_like(pin["q"]).pin_memory()
-        lse_h = torch.empty(tuple(d["lse"].shape), dtype=torch.float32).pin_memory()
-        do_h = torch.empty_like(pin["dq"]).pin_memory()
-        dlse_h = torch.empty(tuple(d["dlse"].shape), dtype=torch.float32).pin_memory()
+        bufs = [d]
+        d2 = {n: torch.empty_like(t) for n, t in d.items()}
+        bufs.append(d2)
+        outs = [dict(o=torch.empty_like(pin["q"]).pin_memory(),
+                     lse=torch.empty(tuple(d["lse"].shape), dtype=torch.float32).pin_memory(),
+                     do=torch.empty_like(pin["dq"]).pin_memory(),
+                     dlse=torch.empty(tuple(d["dlse"].shape), dtype=torch.float32).pin_memory())
+                for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in pin.values())
-        d2h = sum(t.numel() * t.element_size() for t in (o_h, lse_h, do_h, dlse_h))
+        d2h = sum(t.numel() * t.element_size() for t in outs[0].values())
+        s_in, s_cmp, s_out = (torch.cuda.Stream(device) for _ in range(3))
+        ws2 = [ws, torch.empty_like(ws)]
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        cmp_done = [torch.cuda.Event() for _ in range(2)]
+        out_done = [torch.cuda.Event() for _ in range(2)]
 
-        def e2e_step():
-            for n in ("q", "k", "v", "dq", "dk", "dv", "lens"):
-                d[n].copy_(pin[n], non_blocking=True)
-            step()
-            o_h.copy_(d["o"], non_blocking=True)
-            lse_h.copy_(d["lse"], non_blocking=True)
-            do_h.copy_(d["do"], non_blocking=True)
-            dlse_h.copy_(d["dlse"], non_blocking=True)
+        def e2e_step(i):
+            b = i % 2
+            db, ob = bufs[b], outs[b]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(cmp_done[b])  # step i-2 has finished reading buffer b
+                for n in ("q", "k", "v", "dq", "dk", "dv", "lens"):
+                    db[n].copy_(pin[n], non_blocking=True)
+                in_ready[b].record(s_in)
+            s_cmp.wait_event(in_ready[b])
+            if i >= 2:
+                s_cmp.wait_event(out_done[b])  # step i-2's results have left buffer b
+            fa.fa_fwd(db["q"], db["k"], db["v"], causal=wf.causal, scale=wf.scale, out=db["o"],
+                      lse=db["lse"], stream=s_cmp)
+            fa.fa_decode_splitkv(db["dq"], db["dk"], db["dv"], db["lens"], scale=wd.scale,
+                                 num_splits=ns, workspace=ws2[b], out=db["do"], lse=db["dlse"],
+                                 stream=s_cmp)
+            cmp_done[b].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(cmp_done[b])
+                for n in ("o", "lse", "do", "dlse"):
+                    ob[n].copy_(db[n], non_blocking=True)
+                out_done[b].record(s_out)
 
-        e2e_step()
+        for i in range(2):
+            e2e_step(i)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         a0 = torch.cuda.Event(enable_timing=True)
         a1 = torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        a1.record(stream)
+        a0.record(s_in)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        a1.record(s_out)
         torch.cuda.synchronize()
+        if fa.fa_last_device_status() != 0:
+            raise RuntimeError("device status reported a kernel timeout in the end-to-end run")
         e_ms = max_over_ranks(a0.elapsed_time(a1) / args.e2e_steps, world, device)
         e2e = {"value": round(world * fwd_flops / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                "ms_per_step": round(e_ms, 3), "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps}
+               "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
+               "pipelined": "2 buffer sets, upload / compute / download streams"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
