@@ -188,32 +188,6 @@ __device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lb
     return d;
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, one elected thread issues.
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                        uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n"
-        ".reg .pred p;\n"
-        "setp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
-        "}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem], A read from tensor memory (one row per lane).
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                        uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n"
-        ".reg .pred p;\n"
-        "setp.ne.b32 p, %4, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
-        "}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // Lean forms for the issue loop: the accumulate flag is an immediate predicate, and no
 // "memory" clobber (volatile asm statements keep their order relative to the mbarrier
 // waits, which do carry the clobber).
@@ -226,17 +200,6 @@ __device__ __forceinline__ void umma_ss_imm(uint32_t d_tmem, uint64_t adesc, uin
     else
         asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;" ::"r"(d_tmem),
                      "l"(adesc), "l"(bdesc), "r"(idesc));
-}
-
-template <bool kAccumulate>
-__device__ __forceinline__ void umma_ts_imm(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                            uint32_t idesc) {
-    if constexpr (kAccumulate)
-        asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem),
-                     "r"(a_tmem), "l"(bdesc), "r"(idesc));
-    else
-        asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 0;" ::"r"(d_tmem),
-                     "r"(a_tmem), "l"(bdesc), "r"(idesc));
 }
 
 // Warp-uniform issue: the whole warp runs the issue loop and elect.sync picks the lane
