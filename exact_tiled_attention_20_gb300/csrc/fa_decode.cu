@@ -8,10 +8,15 @@
 // is computed independently, writing a partial output and its log-sum-exp, (3) a separate
 // kernel merges them with the log-sum-exp weights.
 //
-// Chunking (the reading of "split the loading across thread blocks" taken here): with
-// L = ceil(max_b kv_lens[b] / num_splits) rounded up to 128, sequence b has
-// n_b = ceil(kv_lens[b] / L) chunks of L keys.  Every (b, kv head, chunk) is one work item
-// of at most L keys, so work items are nearly equal in size whatever the length mix.
+// Splitting (the reading of "split the loading across thread blocks" taken here): the
+// keys of every (sequence b, kv head) pair, in 128-key tiles, are laid end to end in the
+// order (b, kv head), and CTA c takes the tiles [c W, (c + 1) W).  W is the total divided
+// by the grid, so every CTA streams the same number of tiles whatever the length mix,
+// but at least ceil(T_max / (num_splits - 1)) for the longest pair's T_max tiles, so no
+// pair meets more than num_splits ranges.  A pair cut by range boundaries yields one
+// segment per range it meets; each segment is computed independently and writes a
+// partial output and its log-sum-exp into the pair's next slot, which the merge kernel
+// combines.
 //
 // Split kernel (persistent, one CTA per SM, walking the work items):
 //  * the producer warp streams, per item, the Q rows of the query heads sharing the KV head
@@ -39,6 +44,7 @@ struct DecParams {
     const int32_t* kv_lens;
     float* o_part;    // [B, Hq, ns, D]
     float* lse_part;  // [B, Hq, ns]
+    int split_grid;   // CTAs of the split kernel (sets the range width)
     void* o;          // [B, Hq, D]
     float* lse;       // [B, Hq] or null
     int q_rows;  // query-head rows per Q box; rows past q_rows * sq are never read
@@ -89,11 +95,11 @@ struct DecSmemTail {
     alignas(16) float red[2][4][16];   // per-tile cross-warp max, double-buffered
     alignas(16) float lred[4][16];     // end-of-item cross-warp sums
     int lens[kDecMaxB];
-    int prefix[kDecMaxB + 1];  // exclusive prefix of n_b * Hkv
+    int prefix[kDecMaxB + 1];  // exclusive prefix over b of the tiles of one pair of b
     int warp_sums[4];
     int max_len;
-    int chunk;        // L
-    int total_items;
+    int width;        // W, tiles per CTA range
+    int total_tiles;  // Hkv * prefix[B]
     uint32_t tmem_slot;
     int abort_flag;
 };
@@ -104,26 +110,42 @@ constexpr int kDecTileBytes = 2 * kDecNS * kDecKVBytes + 2 * kDecQBytes + 2 * kD
 constexpr int kDecSmemBytes = 1024 + kDecTileBytes + (int)sizeof(DecSmemTail);
 static_assert(kDecSmemBytes <= 232448, "decode shared memory budget");
 
+// One segment of work: keys [k0, k1) of pair (b, hk), written to partial slot c.
 struct DecItem {
     int b, hk, c, k0, k1, ntiles;
 };
 
-__device__ __forceinline__ DecItem decode_item(const DecSmemTail& t, int B, int Hkv, int idx) {
-    int lo = 0, hi = B;  // largest b with prefix[b] <= idx
+// Width W of the CTA ranges (shared by the split and merge kernels, which must agree).
+__device__ __forceinline__ int decode_range_width(int total_tiles, int max_pair_tiles, int grid, int ns) {
+    long long w = ((long long)total_tiles + grid - 1) / grid;
+    if (ns >= 2)
+        w = max(w, ((long long)max_pair_tiles + ns - 2) / (ns - 1));
+    else
+        w = max(w, (long long)total_tiles);  // one range: no pair is cut
+    return (int)max(w, 1LL);
+}
+
+// The next segment of this CTA's range, starting at tile x (x advances past it).
+__device__ __forceinline__ bool next_segment(const DecSmemTail& t, int B, int Hkv, int& x, int end,
+                                             DecItem& it) {
+    if (x >= end) return false;
+    int lo = 0, hi = B;  // largest b with Hkv * prefix[b] <= x; that b has tiles
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (t.prefix[mid] <= idx) lo = mid; else hi = mid;
+        if (Hkv * t.prefix[mid] <= x) lo = mid; else hi = mid;
     }
-    DecItem it;
+    const int tb = t.prefix[lo + 1] - t.prefix[lo];
+    const int hk = (x - Hkv * t.prefix[lo]) / tb;
+    const int pstart = Hkv * t.prefix[lo] + hk * tb;  // first tile of pair (lo, hk)
+    const int seg_end = min(end, pstart + tb);
     it.b = lo;
-    const int nb = (t.prefix[lo + 1] - t.prefix[lo]) / Hkv;
-    const int r = idx - t.prefix[lo];
-    it.hk = r / nb;
-    it.c = r % nb;
-    it.k0 = it.c * t.chunk;
-    it.k1 = min(it.k0 + t.chunk, t.lens[lo]);
-    it.ntiles = (it.k1 - it.k0 + kDecBN - 1) / kDecBN;
-    return it;
+    it.hk = hk;
+    it.c = (int)blockIdx.x - pstart / t.width;  // ranges met by this pair before this one
+    it.k0 = (x - pstart) * kDecBN;
+    it.k1 = min((seg_end - pstart) * kDecBN, t.lens[lo]);
+    it.ntiles = seg_end - x;
+    x = seg_end;
+    return true;
 }
 
 // Shared-memory byte address of P^T[h][key] in the 128-byte-swizzled K-major layout of a
@@ -238,19 +260,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         atomicMax(&T.max_len, len);
     }
     __syncthreads();
-    if (tid == 0) {
-        const int per = (T.max_len + p.ns - 1) / p.ns;
-        T.chunk = max(kDecBN, (per + kDecBN - 1) / kDecBN * kDecBN);
-    }
-    __syncthreads();
     {
-        // exclusive scan of n_b * Hkv over b, 128 threads x up to 8 entries each
+        // exclusive scan over b of the tiles of one pair, 128 threads x up to 8 entries each
         const int per_t = (p.B + 127) / 128;
         int local = 0;
         if (tid < 128) {
             for (int i = 0; i < per_t; ++i) {
                 const int b = tid * per_t + i;
-                if (b < p.B) local += (T.lens[b] + T.chunk - 1) / T.chunk * p.Hkv;
+                if (b < p.B) local += (T.lens[b] + kDecBN - 1) / kDecBN;
             }
         }
         int incl = local;
@@ -268,20 +285,24 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 const int b = tid * per_t + i;
                 if (b < p.B) {
                     T.prefix[b] = run;
-                    run += (T.lens[b] + T.chunk - 1) / T.chunk * p.Hkv;
+                    run += (T.lens[b] + kDecBN - 1) / kDecBN;
                 }
             }
-            if (tid == 127) T.total_items = run;
+            if (tid == 127) T.prefix[p.B] = run;
         }
-        if (tid == 0 && p.B <= 0) T.total_items = 0;
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0) T.prefix[p.B] = T.total_items;
+    if (tid == 0) {
+        T.total_tiles = p.Hkv * T.prefix[p.B];
+        T.width = decode_range_width(T.total_tiles, (T.max_len + kDecBN - 1) / kDecBN, (int)gridDim.x, p.ns);
+    }
     __syncthreads();
     const uint32_t tmem = T.tmem_slot;
-    const int total = T.total_items;
+    // This CTA's range of tiles.
+    const int x0 = (int)min((long long)blockIdx.x * T.width, (long long)T.total_tiles);
+    const int x_end = min(x0 + T.width, T.total_tiles);
     // The merge kernel may be scheduled now; it waits for this grid's results itself.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -292,8 +313,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             bool ok = true;
             // Every K/V row is read exactly once by this kernel.
             const uint64_t kv_policy = l2_policy_evict_first();
-            for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
-                const DecItem it = decode_item(T, p.B, p.Hkv, idx);
+            int x = x0;
+            DecItem it;
+            while (ok && next_segment(T, p.B, p.Hkv, x, x_end, it)) {
                 const uint32_t qs = icount & 1u;
                 ok = mbar_wait(bar(kDBarQEmpty + qs), ((icount >> 1) & 1u) ^ 1u, wc);
                 if (!ok) break;
@@ -379,8 +401,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     umma_ss_imm<true>(tmem + 32, a + (uint64_t)((kk * (16 * 128)) >> 4),
                                       b + (uint64_t)(((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), idesc_o);
             };
-            for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
-                const DecItem item = decode_item(T, p.B, p.Hkv, idx);
+            int x = x0;
+            DecItem item;
+            while (ok && next_segment(T, p.B, p.Hkv, x, x_end, item)) {
                 const int n = item.ntiles;
                 const uint32_t qs = icount & 1u;
                 ok = mbar_wait(bar(kDBarQFull + qs), (icount >> 1) & 1u, wc);
@@ -433,8 +456,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const int g = p.group;
         uint32_t it_s = 0;
         bool ok = true;
-        for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
-            const DecItem item = decode_item(T, p.B, p.Hkv, idx);
+        int x = x0;
+        DecItem item;
+        while (ok && next_segment(T, p.B, p.Hkv, x, x_end, item)) {
             float m_run[GMAX], l_part[GMAX];
 #pragma unroll
             for (int h = 0; h < GMAX; ++h) {
@@ -569,14 +593,21 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 template <bool kBF16>
 __global__ void __launch_bounds__(128)
     fa_decode_combine_kernel(const DecParams p) {
-    __shared__ int s_max_len;
-    if (threadIdx.x == 0) s_max_len = 0;
+    // The split kernel's range width, from the same lengths.
+    __shared__ int s_max_len, s_sum_tiles;
+    if (threadIdx.x == 0) {
+        s_max_len = 0;
+        s_sum_tiles = 0;
+    }
     __syncthreads();
-    for (int b = threadIdx.x; b < p.B; b += blockDim.x)
-        atomicMax(&s_max_len, min(max(p.kv_lens[b], 0), p.Smax));
+    for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+        const int len = min(max(p.kv_lens[b], 0), p.Smax);
+        atomicMax(&s_max_len, len);
+        atomicAdd(&s_sum_tiles, (len + kDecBN - 1) / kDecBN);
+    }
     __syncthreads();
-    const int per = (s_max_len + p.ns - 1) / p.ns;
-    const int L = max(kDecBN, (per + kDecBN - 1) / kDecBN * kDecBN);
+    const int W = decode_range_width(p.Hkv * s_sum_tiles, (s_max_len + kDecBN - 1) / kDecBN,
+                                     p.split_grid, p.ns);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x * 4 + warp;  // row of [B, sq, Hq]
     if (bh >= p.B * p.sq * p.Hq) return;
@@ -584,7 +615,15 @@ __global__ void __launch_bounds__(128)
     const int s_tok = (bh / p.Hq) % p.sq;
     const int hq = bh % p.Hq;
     const int len = min(max(p.kv_lens[b], 0), p.Smax);
-    const int n = (len + L - 1) / L;
+    // This row's pair (b, kv head) starts after the tiles of all earlier pairs; it has one
+    // partial per CTA range it meets.
+    int before = 0;  // tiles of one pair of each sequence before b
+    for (int bb = lane; bb < b; bb += 32) before += (min(max(p.kv_lens[bb], 0), p.Smax) + kDecBN - 1) / kDecBN;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+    const int tb = (len + kDecBN - 1) / kDecBN;
+    const int pstart = p.Hkv * before + (hq / p.group) * tb;
+    const int n = tb > 0 ? (pstart + tb - 1) / W - pstart / W + 1 : 0;
     const float kNegInf = -__int_as_float(0x7f800000);
     const float kLog2e = 1.4426950408889634f;
     const float* lrow = p.lse_part + (size_t)bh * p.ns;
@@ -687,8 +726,9 @@ fa_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
     p.block_table = a.block_table;
     p.page_size = a.page_size;
     p.max_pages = a.max_pages;
-    const long long items_max = (long long)a.B * a.Hkv * a.num_splits;
-    const int grid = (int)(items_max < a.num_sms ? items_max : a.num_sms);
+    // One CTA per SM; the kernel cuts the work into equal ranges of tiles, one per CTA.
+    const int grid = a.num_sms;
+    p.split_grid = grid;
     fa_status st;
     if (g_cols > 16) return FA_ERR_UNSUPPORTED;
     if (g_cols <= 4)

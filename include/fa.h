@@ -123,11 +123,12 @@ FA_API fa_status fa_fwd_varlen(const void *q, const void *k, const void *v, void
 FA_API size_t fa_decode_workspace_bytes(int B, int Hq, int D, int num_splits);
 
 /*
- * The split count fa_decode_splitkv uses when given num_splits <= 0: enough chunks that
- * B * Hkv * num_splits work items cover the GPU several times over, with chunks of at
- * least 256 keys.  max_kv_len is an upper bound on the KV lengths (the cache capacity
- * Smax will do).  num_sms <= 0 queries the current device.  Returns >= 1, or -1 on an
- * invalid argument or when no device can be queried.
+ * The split count fa_decode_splitkv uses when given num_splits <= 0: about eight partials
+ * per SM over the B * Hkv (sequence, kv head) pairs, and no more than one per 256 keys of
+ * max_kv_len.  It bounds how finely a pair may be cut (see num_splits below).  max_kv_len
+ * is an upper bound on the KV lengths (the cache capacity Smax will do).  num_sms <= 0
+ * queries the current device.  Returns >= 1, or -1 on an invalid argument or when no
+ * device can be queried.
  */
 FA_API int fa_decode_default_splits(int B, int Hkv, int max_kv_len, int num_sms);
 
@@ -137,10 +138,12 @@ FA_API int fa_decode_default_splits(int B, int Hkv, int max_kv_len, int num_sms)
  *   kv_lens  device int32 [B], 0 <= kv_lens[b] <= Smax: sequence b attends to cache
  *            positions [0, kv_lens[b]).  kv_lens[b] == 0 gives o = 0, lse = -inf.
  *   o        [B, 1, Hq, D] (dtype)      lse [B, Hq] fp32 (may be NULL)
- *   num_splits  the most chunks any sequence is cut into (<= 0: the default above).
- *            With L = the longest kv_lens[] divided by num_splits, rounded up to a multiple
- *            of 128, sequence b is cut into ceil(kv_lens[b] / L) chunks of L keys; every
- *            chunk is one work item, and a second kernel merges each sequence's chunks.
+ *   num_splits  the most pieces any (sequence, kv head) pair is cut into (<= 0: the
+ *            default above).  The keys of all pairs, in 128-key tiles, are laid end to end
+ *            in (b, kv head) order and cut into one equal range of W tiles per SM, W at
+ *            least ceil(T / (num_splits - 1)) for the longest pair's T tiles (with
+ *            num_splits == 1 no pair is cut).  Each piece of a pair writes a partial
+ *            output and log-sum-exp, and a second kernel merges each pair's pieces.
  *   workspace   device memory of at least fa_decode_workspace_bytes(B, Hq, D, num_splits)
  *            bytes (after the default is applied); its contents need no initialisation.
  * Sizes: B, Hq, Hkv, Smax >= 1; B <= 1024; D == 128; Hq % Hkv == 0; Hq / Hkv <= 16.

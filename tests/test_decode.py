@@ -1,8 +1,8 @@
 """GPU parity of fa_decode_splitkv (split-KV single-token decode) against the CPU oracle.
 
 Bars: max|dO| <= 1e-2, max|dLSE| <= 1e-3 against the fp64 definition (oracle.decode),
-element by element.  The per-chunk partials in the workspace are checked against the
-oracle's attention over each chunk's key range (oracle.partial), and the merged output
+element by element.  The per-piece partials in the workspace are checked against the
+oracle's attention over each piece's key range (oracle.partial), and the merged output
 against the full definition, for several split counts, zero-length caches, group sizes
 1..16, fp16, and the full-size decode workload (every output).
 """
@@ -50,9 +50,29 @@ def _check(o, lse, o_ref, lse_ref):
     return do, dl
 
 
-def _chunk_len(lens, ns):
-    per = (int(max(lens)) + ns - 1) // ns
-    return max(128, (per + 127) // 128 * 128)
+def _pieces(lens, Hkv, ns, grid):
+    """Key ranges of the split kernel's partials, as the API documents them: the 128-key
+    tiles of all (sequence, kv head) pairs laid end to end in (b, kv head) order and cut
+    into ranges of W tiles, one per CTA.  Returns {(b, hk): [(slot, k0, k1), ...]}."""
+    tiles = [(n + 127) // 128 for n in lens]
+    prefix = [0]
+    for t in tiles:
+        prefix.append(prefix[-1] + t)
+    total = Hkv * prefix[-1]
+    w = (total + grid - 1) // grid
+    w = max(w, (max(tiles) + ns - 2) // (ns - 1)) if ns >= 2 else max(w, total)
+    w = max(w, 1)
+    out = {}
+    for b, tb in enumerate(tiles):
+        for hk in range(Hkv):
+            start = Hkv * prefix[b] + hk * tb
+            x, pieces = start, []
+            while x < start + tb:
+                end = min((x // w + 1) * w, start + tb)
+                pieces.append((x // w - start // w, (x - start) * 128, min((end - start) * 128, lens[b])))
+                x = end
+            out[(b, hk)] = pieces
+    return out
 
 
 @pytest.mark.parametrize("ns", [1, 2, 3, 7, 16])
@@ -66,11 +86,12 @@ def test_decode_matches_oracle(fa, ns):
     _check(o, lse, o_ref, lse_ref)
 
 
-def test_decode_partials_match_oracle_chunks(fa):
-    """The workspace holds, per (b, head, chunk), the chunk's own attention and LSE."""
-    B, Hq, Hkv, D, Smax, ns = 2, 8, 2, 128, 900, 4
-    q, kc, vc, _ = inputs.make_decode(B, Hq, Hkv, D, Smax, 1, Smax, seed=61)
-    lens = torch.tensor([900, 250], dtype=torch.int32)
+@pytest.mark.parametrize("ns", [2, 4, 64])
+def test_decode_partials_match_oracle_pieces(fa, ns):
+    """The workspace holds, per (b, head, piece), the piece's own attention and LSE."""
+    B, Hq, Hkv, D, Smax = 3, 8, 2, 128, 3000
+    q, kc, vc, _ = inputs.make_decode(B, Hq, Hkv, D, Smax, 1, Smax, seed=61 + ns)
+    lens = torch.tensor([3000, 250, 1300], dtype=torch.int32)
     nbytes = fa.fa_decode_workspace_bytes(B, Hq, D, ns)
     ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda:0")
     fa.fa_decode_splitkv(*_dev(q, kc, vc, lens), num_splits=ns, workspace=ws)
@@ -79,16 +100,20 @@ def test_decode_partials_match_oracle_chunks(fa):
     o_bytes = (rows * D * 4 + 255) // 256 * 256
     o_part = ws[: rows * D * 4].view(torch.float32).view(B, Hq, ns, D).cpu().numpy()
     l_part = ws[o_bytes: o_bytes + rows * 4].view(torch.float32).view(B, Hq, ns).cpu().numpy()
-    L = _chunk_len(lens.tolist(), ns)
+    grid = torch.cuda.get_device_properties(0).multi_processor_count
+    pieces = _pieces(lens.tolist(), Hkv, ns, grid)
     scale = 1 / math.sqrt(D)
+    g = Hq // Hkv
+    checked = 0
     for b in range(B):
-        n_b = (int(lens[b]) + L - 1) // L
         for h in range(Hq):
-            for c in range(n_b):
-                j0, j1 = c * L, min((c + 1) * L, int(lens[b]))
+            for slot, j0, j1 in pieces[(b, h // g)]:
+                assert slot < ns
                 o_ref, l_ref = oracle.partial(q, kc, vc, b, h, j0, j1, scale)
-                assert np.abs(o_part[b, h, c] - o_ref).max() <= O_TOL
-                assert abs(l_part[b, h, c] - l_ref) <= LSE_TOL
+                assert np.abs(o_part[b, h, slot] - o_ref).max() <= O_TOL
+                assert abs(l_part[b, h, slot] - l_ref) <= LSE_TOL
+                checked += 1
+    assert checked >= B * Hq
 
 
 def test_decode_empty_and_single_key_sequences(fa):
