@@ -79,7 +79,7 @@ struct FwdConfig {
     static constexpr int kOCol0 = kSlots * BN;        // first O column in TMEM
     static constexpr int kTmemCols = 512;
     static_assert(kOCol0 + NQ * D <= kTmemCols, "TMEM budget");
-    static_assert(D % 32 == 0 && BN % 64 == 0, "tile shape");
+    static_assert(D % 32 == 0 && BN % 32 == 0, "tile shape");
     static constexpr int kThreads = 128 * NQ + 64;
     // O-done is signalled after every P.V when S is issued ahead of P.V (NQ == 1), and
     // only after a tile's last P.V otherwise.
