@@ -226,6 +226,8 @@ fa_status decode_common(const void* q, const void* k_cache, const void* v_cache,
     if (Sq <= 0) return FA_ERR_INVALID_ARG;
     if ((Hq / Hkv) * Sq > 16 || B > 1024) return FA_ERR_UNSUPPORTED;
     if ((long long)B * Smax > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+    // The kernels count 128-key tiles over all (sequence, kv head) pairs in 32 bits.
+    if ((long long)B * ((Smax + 127) / 128) * Hkv > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
     DeviceInfo di;
     if (!device_info(&di)) return FA_ERR_CUDA;
     if (num_splits <= 0) num_splits = fa_decode_default_splits(B, Hkv, Smax, di.num_sms);

@@ -90,6 +90,8 @@ def test_decode_argument_validation(lib):
     assert L.fa_decode_splitkv(*bad) == 2
     bad = list(base); bad[7] = 64; bad[8] = 2                            # group of 32 > 16
     assert L.fa_decode_splitkv(*bad) == 2
+    bad = list(base); bad[6] = 1024; bad[7] = 256; bad[8] = 256; bad[10] = 1 << 20
+    assert L.fa_decode_splitkv(*bad) == 2                                # 2^31 tiles over all pairs
 
 
 def test_valid_call_without_a_device_fails_loudly(lib):
