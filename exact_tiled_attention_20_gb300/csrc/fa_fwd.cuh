@@ -43,7 +43,12 @@ struct FwdParams {
     int has_lo, win_left, has_hi, hi_off;
     float scale_log2;  // softmax scale * log2(e)
     int num_qb;        // query blocks of NQ * 128 rows per (b, h) (fixed-length batches)
-    int num_tiles;     // B * Hq * num_qb (fixed-length batches)
+    int num_tiles;     // tile indices the CTAs walk (fixed-length batches)
+    // Causal fixed-length batches: query blocks qb and num_qb - 1 - qb of a head, whose
+    // key ranges add up to the same length for every qb, go to the same CTA one after the
+    // other, so every CTA gets the same work.  Tile index t = (2 v + m) * grid + c names
+    // pair v * grid + c, member m (0: the long block, 1: the short one).
+    int pair_tiles;
     // Variable-length batches (page "flash-attention-v100", "Changelog", "2.0",
     // flash_attn_varlen_func): sequence b holds query rows [cu_q[b], cu_q[b+1]) of a packed
     // [total_q, Hq, D] tensor and key rows [cu_k[b], cu_k[b+1]) of [total_k, Hkv, D];
@@ -110,7 +115,7 @@ struct FwdConfig {
 };
 
 struct TileCoord {
-    int b, h, hk, m0, j0, n_kv;  // K/V blocks j0 .. j0 + n_kv - 1
+    int b, h, hk, m0, j0, n_kv;  // K/V blocks j0 .. j0 + n_kv - 1; n_kv < 0: no such tile
     int sq, sk;                  // this sequence's query and key lengths
     int q_base, k_base, tb;      // TMA row offsets and outer coordinate of the sequence
     long long o_row0;            // packed output row of query 0 of this sequence
@@ -142,8 +147,25 @@ __device__ __forceinline__ TileCoord decode_tile(const FwdParams& p, const Varle
         c.lse0 = (long long)c.h * p.total_q + vt->q0[lo];
     } else {
         nqb = p.num_qb;
-        qb_raw = t % nqb;
-        const int bh = t / nqb;
+        int bh;
+        if (p.pair_tiles) {
+            const int g = (int)gridDim.x;
+            const int w = t / g;
+            const int pairs = (nqb + 1) >> 1;
+            const int v = (w >> 1) * g + (t - w * g);
+            bh = v / pairs;
+            const int k = v - bh * pairs;
+            // qb_raw counts from the longest block; member 1 of the middle block of an odd
+            // count, and pairs past the last head, are not tiles.
+            qb_raw = (w & 1) ? nqb - 1 - k : k;
+            if (bh >= p.B * p.Hq || ((w & 1) && nqb - 1 - k == k)) {
+                c.n_kv = -1;
+                return c;
+            }
+        } else {
+            qb_raw = t % nqb;
+            bh = t / nqb;
+        }
         c.h = bh % p.Hq;
         c.b = bh / p.Hq;
         c.sq = p.Sq;
@@ -244,7 +266,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 const TileCoord c = decode_tile<C>(p, vtab, t);
-                if (c.n_kv == 0) continue;
+                if (c.n_kv <= 0) continue;
                 for (int q = 0; q < C::NQ && ok; ++q) {
                     ok = mbar_wait(bar(C::kBarQEmpty + q), (tcount & 1u) ^ 1u, wc);
                     if (!ok) break;
@@ -343,7 +365,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 const TileCoord c = decode_tile<C>(p, vtab, t);
                 const int n = c.n_kv;
-                if (n == 0) continue;
+                if (n <= 0) continue;
                 for (int q = 0; q < C::NQ && ok; ++q) ok = wait(bar(C::kBarQFull + q), tcount & 1u);
                 if (!ok) break;
                 {
@@ -430,6 +452,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             const bool row_ok = row < c.sq && c.o_row0 + row >= 0 && c.o_row0 + row < p.total_q;
             const size_t o_row = (size_t)(c.o_row0 + row) * p.Hq + c.h;
             uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + o_row * C::D;
+            if (c.n_kv < 0) continue;  // not a tile (causal pairing)
             if (c.n_kv == 0) {
                 if (row_ok) {
 #pragma unroll
@@ -610,6 +633,35 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     }
 }
 
+// Causal tile walk: whether pairing long and short query blocks (FwdParams::pair_tiles)
+// leaves the busiest CTA less work than dealing the blocks out longest first.  Query block
+// qb of a head covers about qb + 1 of its key spans; each tile also costs about half a
+// span of fixed overhead.  Both walks are replayed, over up to 2^18 tiles; beyond that
+// many tiles per CTA even out either way and pairing is kept.
+inline bool causal_pairs_balance_better(long long heads, int nqb, int sms) {
+    const long long tiles = heads * nqb;
+    const long long pairs = heads * ((nqb + 1) / 2);
+    if (tiles > (1LL << 18) || sms > 1024) return true;
+    const int g_rr = (int)(tiles < sms ? tiles : sms);
+    const int g_pr = (int)(pairs < sms ? pairs : sms);
+    static thread_local long long load[1024];
+    for (int i = 0; i < g_rr; ++i) load[i] = 0;
+    for (long long t = 0; t < tiles; ++t) load[t % g_rr] += 2 * (nqb - (t % nqb)) + 1;
+    long long max_rr = 0;
+    for (int i = 0; i < g_rr; ++i) max_rr = load[i] > max_rr ? load[i] : max_rr;
+    for (int i = 0; i < g_pr; ++i) load[i] = 0;
+    const int per = (nqb + 1) / 2;
+    for (long long v = 0; v < pairs; ++v) {
+        const int k = (int)(v % per);
+        long long w = 2 * (nqb - k) + 1;             // the long block, qb = nqb - 1 - k
+        if (nqb - 1 - k != k) w += 2 * (k + 1) + 1;  // the short one, qb = k
+        load[v % g_pr] += w;
+    }
+    long long max_pr = 0;
+    for (int i = 0; i < g_pr; ++i) max_pr = load[i] > max_pr ? load[i] : max_pr;
+    return max_pr < max_rr;
+}
+
 // Host launcher for one configuration.
 template <class C>
 fa_status launch_fwd_cfg(const FwdArgs& a, cudaStream_t stream) {
@@ -639,6 +691,7 @@ fa_status launch_fwd_cfg(const FwdArgs& a, cudaStream_t stream) {
     p.has_hi = (a.causal || a.window_right >= 0) ? 1 : 0;
     p.hi_off = a.causal ? 0 : (a.window_right >= 0 ? a.window_right : 0);
     p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.pair_tiles = 0;
     p.cu_q = a.cu_q;
     p.cu_k = a.cu_k;
     p.total_q = varlen ? a.total_q : a.B * a.Sq;  // packed rows of O (the store guard)
@@ -649,6 +702,16 @@ fa_status launch_fwd_cfg(const FwdArgs& a, cudaStream_t stream) {
         if (tiles > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
         p.num_tiles = (int)tiles;
         grid = p.num_tiles < a.num_sms ? p.num_tiles : a.num_sms;
+        if (a.causal && a.window_left < 0 && p.num_qb > 1 &&
+            causal_pairs_balance_better((long long)a.B * a.Hq, p.num_qb, a.num_sms)) {
+            // causal: query blocks go out in long/short pairs, one pair per CTA at a time
+            const long long pairs = (long long)a.B * a.Hq * ((p.num_qb + 1) / 2);
+            grid = pairs < a.num_sms ? (int)pairs : a.num_sms;
+            const long long walked = 2LL * grid * ((pairs + grid - 1) / grid);
+            if (walked > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+            p.num_tiles = (int)walked;
+            p.pair_tiles = 1;
+        }
     } else {
         p.num_qb = 0;
         p.num_tiles = 0;  // counted on the device from cu_seqlens
