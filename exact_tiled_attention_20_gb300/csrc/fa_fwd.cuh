@@ -44,10 +44,10 @@ struct FwdParams {
     float scale_log2;  // softmax scale * log2(e)
     int num_qb;        // query blocks of NQ * 128 rows per (b, h) (fixed-length batches)
     int num_tiles;     // tile indices the CTAs walk (fixed-length batches)
-    // Causal fixed-length batches: query blocks qb and num_qb - 1 - qb of a head, whose
-    // key ranges add up to the same length for every qb, go to the same CTA one after the
-    // other, so every CTA gets the same work.  Tile index t = (2 v + m) * grid + c names
-    // pair v * grid + c, member m (0: the long block, 1: the short one).
+    // Causal batches: query blocks qb and nqb - 1 - qb of a (sequence, head), whose key
+    // ranges add up to the same length for every qb, go to the same CTA one after the
+    // other, so CTAs get even work.  Tile index t = (2 v + m) * grid + c names pair
+    // v * grid + c, member m (0: the long block, 1: the short one).
     int pair_tiles;
     // Variable-length batches (page "flash-attention-v100", "Changelog", "2.0",
     // flash_attn_varlen_func): sequence b holds query rows [cu_q[b], cu_q[b+1]) of a packed
@@ -127,18 +127,40 @@ __device__ __forceinline__ TileCoord decode_tile(const FwdParams& p, const Varle
     TileCoord c;
     int qb_raw, bh_local, nqb;
     if (vt) {
-        int lo = 0, hi = p.B;  // largest b with prefix[b] <= t
+        // With pairing the prefix counts pairs of query blocks (see pair_tiles).
+        int u = t, w = 0;
+        if (p.pair_tiles) {
+            const int g = (int)gridDim.x;
+            w = t / g;
+            u = (w >> 1) * g + (t - w * g);
+            if (u >= vt->prefix[p.B]) {
+                c.n_kv = -1;
+                return c;
+            }
+        }
+        int lo = 0, hi = p.B;  // largest b with prefix[b] <= u
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (vt->prefix[mid] <= t) lo = mid; else hi = mid;
+            if (vt->prefix[mid] <= u) lo = mid; else hi = mid;
         }
         c.b = lo;
         c.sq = vt->q0[lo + 1] - vt->q0[lo];
         c.sk = vt->k0[lo + 1] - vt->k0[lo];
         nqb = (c.sq + C::NQ * C::BM - 1) / (C::NQ * C::BM);
-        const int local = t - vt->prefix[lo];
-        qb_raw = local % nqb;
-        bh_local = local / nqb;
+        const int local = u - vt->prefix[lo];
+        if (p.pair_tiles) {
+            const int pairs = (nqb + 1) >> 1;
+            bh_local = local / pairs;
+            const int k = local - bh_local * pairs;
+            qb_raw = (w & 1) ? nqb - 1 - k : k;
+            if ((w & 1) && nqb - 1 - k == k) {
+                c.n_kv = -1;
+                return c;
+            }
+        } else {
+            qb_raw = local % nqb;
+            bh_local = local / nqb;
+        }
         c.h = bh_local;
         c.q_base = vt->q0[lo];
         c.k_base = vt->k0[lo];
@@ -248,7 +270,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             for (int b = 0; b < p.B; ++b) {
                 vtab->prefix[b] = run;
                 const int sq = max(vtab->q0[b + 1] - vtab->q0[b], 0);
-                run += p.Hq * ((sq + C::NQ * C::BM - 1) / (C::NQ * C::BM));
+                const int nqb = (sq + C::NQ * C::BM - 1) / (C::NQ * C::BM);
+                run += p.Hq * (p.pair_tiles ? (nqb + 1) / 2 : nqb);
             }
             vtab->prefix[p.B] = run;
         }
@@ -256,7 +279,13 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (vtab) num_tiles = vtab->prefix[p.B];
+    if (vtab) {
+        num_tiles = vtab->prefix[p.B];
+        if (p.pair_tiles) {  // two members per pair, walked a grid-wide wave at a time
+            const int g = (int)gridDim.x;
+            num_tiles = 2 * g * ((num_tiles + g - 1) / g);
+        }
+    }
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
     if (warp == C::kProducerWarp) {
@@ -715,6 +744,8 @@ fa_status launch_fwd_cfg(const FwdArgs& a, cudaStream_t stream) {
     } else {
         p.num_qb = 0;
         p.num_tiles = 0;  // counted on the device from cu_seqlens
+        // causal: pair long and short query blocks of each (sequence, head)
+        p.pair_tiles = (a.causal && a.window_left < 0) ? 1 : 0;
     }
     p.o = a.o;
     p.lse = a.lse;
