@@ -93,6 +93,18 @@ def test_fwd_causal_bottom_right_edges(fa, sq, sk):
         assert torch.all(o[:, : sq - sk] == 0)
 
 
+@pytest.mark.parametrize("sq,sk", [(2700, 2700), (2700, 3000)])
+def test_fwd_causal_paired_walk(fa, sq, sk):
+    """Causal batches walk query blocks qb and nqb-1-qb of a head back to back when that
+    balances the CTAs better.  This shape (16 heads, 11 query blocks of 256 rows each, the
+    last one ragged) takes the paired walk with an odd block count, where the middle
+    block has no partner; every row is checked."""
+    q, k, v = inputs.make_qkv(2, sq, sk, 8, 2, 128, seed=sq + sk)
+    o, lse = _run(fa, q, k, v, True)
+    o_ref, lse_ref = oracle.fwd(q, k, v, scale=1 / math.sqrt(128), causal=True)
+    _compare(o, lse, o_ref, lse_ref)
+
+
 def test_fwd_fp16(fa):
     q, k, v = inputs.make_qkv(1, 260, 260, 4, 2, 128, seed=21, dtype="fp16")
     for causal in (False, True):
