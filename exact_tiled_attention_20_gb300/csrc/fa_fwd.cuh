@@ -9,9 +9,12 @@
 // the RTX 3080 kernel there is prior art, this is a Blackwell design):
 //  * A persistent CTA per SM walks work tiles (b, h, query block of NQ x 128 rows); the
 //    query blocks of one head are adjacent in the walk so concurrent CTAs share K/V in L2.
+//    In causal batches a CTA takes query blocks qb and nqb - 1 - qb of a head back to
+//    back: their key ranges add up to the same length, so the CTAs get even work.
 //  * Warp roles: one TMA producer warp streams Q once per tile and K/V tiles of BN keys
-//    through an NS-stage ring (full / empty mbarriers); one MMA warp issues tcgen05.mma;
-//    NQ softmax warpgroups own one 128-row Q tile each (thread = row = TMEM lane).
+//    through an NS-stage ring (full / empty mbarriers); one MMA warp issues tcgen05.mma
+//    (the whole warp runs the issue loop, elect.sync picks the issuing lane); NQ softmax
+//    warpgroups own one 128-row Q tile each (thread = row = TMEM lane).
 //  * S = Q K^T: A = Q and B = K from 128-byte-swizzled shared memory, fp32 accumulator in
 //    TMEM.  The softmax warpgroup reads S from TMEM, applies the mask, keeps the running
 //    max m and sum l (online softmax in base 2 with scale*log2(e) folded into one FMA),
