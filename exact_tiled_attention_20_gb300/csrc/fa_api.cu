@@ -193,8 +193,8 @@ int fa_decode_default_splits(int B, int Hkv, int max_kv_len, int num_sms) {
         if (!device_info(&di)) return -1;
         num_sms = di.num_sms;
     }
-    // Aim for about eight work items per SM (lengths vary, so about half the chunks of
-    // the longest sequence exist for an average one), with chunks of at least 256 keys.
+    // Allow about eight pieces per SM over the (sequence, kv head) pairs, and no more than
+    // one piece per 256 keys of the longest sequence.
     const long long groups = (long long)B * Hkv;
     long long ns = (8LL * num_sms + groups - 1) / groups;
     const long long max_by_len = ((long long)max_kv_len + 255) / 256;

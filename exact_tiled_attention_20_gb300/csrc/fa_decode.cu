@@ -637,14 +637,14 @@ __global__ void __launch_bounds__(128)
     for (int c = lane; c < n; c += 32) m = fmaxf(m, lrow[c]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    // m = -inf: no chunk holds a visible key for this row (empty cache, or a causal token
+    // m = -inf: no piece holds a visible key for this row (empty cache, or a causal token
     // that sees none): O = 0, LSE = -inf.
     if (n > 0 && m != kNegInf) {
         float s = 0.f;
         for (int c = lane; c < n; c += 32) s += ex2_approx((lrow[c] - m) * kLog2e);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        // fixed summation order over the chunks; four loads in flight per lane
+        // fixed summation order over the pieces; four loads in flight per lane
         int c = 0;
         for (; c + 4 <= n; c += 4) {
             float4 v[4];

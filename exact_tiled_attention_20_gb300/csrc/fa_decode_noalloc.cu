@@ -1,7 +1,7 @@
 // fa_decode_noalloc.cu -- split-KV decode with library-owned scratch, for callers that
 // cannot allocate device memory.
 //
-// fa_decode_splitkv needs a workspace for its per-chunk partial results, which the caller
+// fa_decode_splitkv needs a workspace for its per-piece partial results, which the caller
 // normally allocates.  Some callers cannot: a plugin running inside a host runtime that
 // owns every device allocation, or a latency-critical serving loop that must never call
 // cudaMalloc (which may synchronise the device).  For them this file keeps the workspace

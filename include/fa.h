@@ -13,7 +13,7 @@
  *                     that tiles Q row blocks over thread blocks and streams K/V tiles).
  *
  *  fa_decode_splitkv  single-token decode over a KV cache with per-sequence lengths, the KV
- *                     range cut into chunks processed by different thread blocks, each
+ *                     range cut into pieces processed by different thread blocks, each
  *                     writing a partial output and its log-sum-exp, then merged by a
  *                     separate kernel.  Page "flash-attention-v100", "Changelog",
  *                     "2.2: Optimize for inference" and flash_attn_with_kvcache
@@ -184,7 +184,7 @@ FA_API fa_status fa_decode_splitkv_multi(const void *q, const void *k_cache, con
  * accepted).  Table entries outside [0, num_pages) for pages a sequence uses are the
  * caller's error: those keys read as zeros, never outside the pool.  Everything else,
  * including the workspace (fa_decode_workspace_bytes(B, Hq, D, num_splits)) and the
- * chunking, is as fa_decode_splitkv with Smax = page_size * max_pages_per_seq.
+ * split into pieces, is as fa_decode_splitkv with Smax = page_size * max_pages_per_seq.
  */
 FA_API fa_status fa_decode_splitkv_paged(const void *q, const void *k_pages, const void *v_pages,
                                          const int32_t *block_table, const int32_t *kv_lens,
