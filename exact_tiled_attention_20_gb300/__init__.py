@@ -12,18 +12,18 @@ generators (``inputs``).  The binding's names mirror the C entry points:
 * ``fa_decode_splitkv_paged`` -- the same over a paged KV cache with a block table;
 * ``fa_decode_splitkv_noalloc`` -- decode with library-owned scratch (no workspace);
 * ``fa_decode_workspace_bytes``, ``fa_decode_default_splits``, ``fa_status_string``,
-  ``fa_last_device_status``.
+  ``fa_last_device_status``, ``fa_selftest_bounded_wait`` (the bounded-wait self-test).
 
 Importing the package does not load the library; the first call does, and raises if
 ``libfa.so`` has not been built.
 """
 from ._lib import (FA_BF16, FA_FP16, FaError, fa_decode_default_splits, fa_decode_splitkv,
                    fa_decode_splitkv_multi, fa_decode_splitkv_noalloc, fa_decode_splitkv_paged, fa_decode_workspace_bytes,
-                   fa_fwd, fa_fwd_varlen, fa_last_device_status, fa_status_string, library_path,
-                   load)
+                   fa_fwd, fa_fwd_varlen, fa_last_device_status, fa_selftest_bounded_wait,
+                   fa_status_string, library_path, load)
 
 __all__ = [
     "FA_BF16", "FA_FP16", "FaError", "fa_fwd", "fa_fwd_varlen", "fa_decode_splitkv", "fa_decode_splitkv_paged",
     "fa_decode_splitkv_noalloc", "fa_decode_splitkv_multi", "fa_decode_workspace_bytes", "fa_decode_default_splits",
-    "fa_status_string", "fa_last_device_status", "library_path", "load",
+    "fa_status_string", "fa_last_device_status", "fa_selftest_bounded_wait", "library_path", "load",
 ]

@@ -62,6 +62,8 @@ def load():
         lib.fa_status_string.restype = ctypes.c_char_p
         lib.fa_last_device_status.argtypes = []
         lib.fa_last_device_status.restype = I
+        lib.fa_selftest_bounded_wait.argtypes = [P, P]
+        lib.fa_selftest_bounded_wait.restype = I
         _lib = lib
         return lib
 
@@ -87,6 +89,16 @@ def fa_status_string(status: int) -> str:
 def fa_last_device_status() -> int:
     """Reads and clears the device status word (synchronises the device)."""
     return int(load().fa_last_device_status())
+
+
+def fa_selftest_bounded_wait(result, stream=None) -> int:
+    """Enqueues the bounded-wait self-test (see include/fa.h); result is a CUDA int32
+    tensor of 3 elements.  Returns the launch status."""
+    _check_cuda("result", result, torch.int32)
+    if result.numel() < 3:
+        raise ValueError("result needs 3 elements")
+    return int(load().fa_selftest_bounded_wait(ctypes.c_void_p(result.data_ptr()),
+                                               ctypes.c_void_p(_stream_handle(stream))))
 
 
 def fa_fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,

@@ -1,4 +1,5 @@
-// fa_api.cu -- the C ABI: argument validation, TMA tensor-map encoding, dispatch.
+// fa_api.cu -- the C ABI: argument validation, TMA tensor-map encoding, dispatch, and the
+// self-test of the bounded barrier wait.
 //
 // Nothing here allocates device memory.  Every call validates its arguments before it
 // enqueues anything, launches on the caller's stream and returns without synchronising.
@@ -11,6 +12,7 @@
 #include <mutex>
 
 #include "fa_internal.h"
+#include "fa_ptx.cuh"
 
 namespace fa {
 
@@ -102,6 +104,43 @@ bool ensure_smem_attr(const void* func, int bytes, int* done_flags) {
         return false;
     __atomic_store_n(&done_flags[dev], 1, __ATOMIC_RELEASE);
     return true;
+}
+
+// Self-test of the bounded wait that every kernel's barrier waits go through.  Warp 0
+// waits on a barrier phase that nothing completes until the wait limit passes; it then
+// records the timeout and raises the CTA abort flag.  Warp 1 starts its own such wait half
+// a second later and must leave on that flag, before its own limit.  Lane 0 of each warp
+// writes: result[0] = warp 0 gave up, result[1] = warp 1 left on the flag, result[2] =
+// warp 0's wait in ms.
+__global__ void __launch_bounds__(64, 1) selftest_bounded_wait_kernel(int* result, int* status) {
+    __shared__ uint64_t bars[2];
+    __shared__ int abort_flag;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bars[0]), 1);
+        mbar_init(smem_u32(&bars[1]), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const WaitCtx wc{&abort_flag, status};
+    if (warp == 1) {  // a bounded delay, so that warp 0's limit passes first
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < kWaitLimitNs / 4) {
+        }
+    }
+    const uint64_t t0 = globaltimer_ns();
+    const bool ok = mbar_wait(smem_u32(&bars[warp]), 0, wc);
+    const uint64_t waited = globaltimer_ns() - t0;
+    if (lane == 0) {
+        if (warp == 0) {
+            result[0] = ok ? 0 : 1;
+            result[2] = (int)(waited / 1000000ull);
+        } else {
+            result[1] = (!ok && waited < kWaitLimitNs) ? 1 : 0;
+        }
+    }
 }
 
 }  // namespace fa
@@ -290,6 +329,14 @@ const char* fa_status_string(fa_status s) {
         case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel gave up on a bounded wait";
         default: return "unknown fa_status";
     }
+}
+
+fa_status fa_selftest_bounded_wait(int* result, fa_stream_t stream) {
+    if (!result || !aligned16(result)) return FA_ERR_INVALID_ARG;
+    DeviceInfo di;
+    if (!device_info(&di)) return FA_ERR_CUDA;
+    selftest_bounded_wait_kernel<<<1, 64, 0, (cudaStream_t)stream>>>(result, di.status);
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_last_device_status(void) {

@@ -231,6 +231,22 @@ FA_API const char *fa_status_string(fa_status s);
  */
 FA_API fa_status fa_last_device_status(void);
 
+/*
+ * Self-test of the bounded-wait path that every kernel's barrier waits use.  Enqueues one
+ * CTA of two warps on `stream`.  Warp 0 waits on an mbarrier phase that no thread
+ * completes.  After the wait limit (2 s of GPU time) it gives up, records FA_ERR_TIMEOUT in
+ * the device status word and raises the CTA's abort flag.  Warp 1 starts the same kind of
+ * wait 0.5 s later and leaves when it sees the flag.  Nothing faults: every wait ends by
+ * itself, and the context stays usable.
+ *   result  device int32[3], caller-owned, 16-byte aligned.  It receives:
+ *           [0] 1 if warp 0's wait gave up;
+ *           [1] 1 if warp 1 left on the abort flag before its own limit;
+ *           [2] warp 0's wait in milliseconds.
+ * Read the status afterwards with fa_last_device_status(), which also clears it.
+ * FA_ERR_INVALID_ARG for a null or misaligned result; FA_ERR_CUDA if the launch failed.
+ */
+FA_API fa_status fa_selftest_bounded_wait(int *result, fa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

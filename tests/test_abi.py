@@ -94,6 +94,13 @@ def test_decode_argument_validation(lib):
     assert L.fa_decode_splitkv(*bad) == 2                                # 2^31 tiles over all pairs
 
 
+def test_selftest_argument_validation(lib):
+    L = lib[0]
+    L.fa_selftest_bounded_wait.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    assert L.fa_selftest_bounded_wait(None, None) == 1       # null result
+    assert L.fa_selftest_bounded_wait(FAKE + 4, None) == 1   # misaligned result
+
+
 def test_valid_call_without_a_device_fails_loudly(lib):
     """With arguments that pass validation but no usable GPU, the call reports
     FA_ERR_CUDA; there is no CPU fallback."""
