@@ -193,6 +193,31 @@ def test_decode_full_size_workload(fa):
     _check(o, lse, o_ref, lse_ref)
 
 
+def test_decode_output_and_workspace_guard_bands(fa):
+    """Writes stay inside O, LSE and the workspace: sentinel pages around each are
+    untouched, including with an empty sequence and a length one past a tile."""
+    B, Hq, Hkv, D, Smax, ns = 3, 8, 2, 128, 900, 4
+    q, kc, vc, _ = inputs.make_decode(B, Hq, Hkv, D, Smax, 1, Smax, seed=91)
+    lens = torch.tensor([900, 0, 129], dtype=torch.int32)
+    dev = torch.device("cuda:0")
+    pad = 4096
+    n_o, n_l = B * Hq * D, B * Hq
+    nbytes = fa.fa_decode_workspace_bytes(B, Hq, D, ns)
+    o_buf = torch.full((pad + n_o + pad,), 7.0, dtype=torch.bfloat16, device=dev)
+    l_buf = torch.full((pad + n_l + pad,), 7.0, dtype=torch.float32, device=dev)
+    w_buf = torch.full((pad + nbytes + pad,), 0xA5, dtype=torch.uint8, device=dev)
+    o = o_buf[pad:pad + n_o].view(B, 1, Hq, D)
+    lse = l_buf[pad:pad + n_l].view(B, Hq)
+    fa.fa_decode_splitkv(*_dev(q, kc, vc, lens), num_splits=ns, workspace=w_buf[pad:pad + nbytes],
+                         out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(o_buf[:pad] == 7.0) and torch.all(o_buf[-pad:] == 7.0)
+    assert torch.all(l_buf[:pad] == 7.0) and torch.all(l_buf[-pad:] == 7.0)
+    assert torch.all(w_buf[:pad] == 0xA5) and torch.all(w_buf[-pad:] == 0xA5)
+    o_ref, lse_ref = oracle.decode(q, kc, vc, lens, scale=1 / math.sqrt(D))
+    _check(o, lse, o_ref, lse_ref)
+
+
 def test_decode_rejects_bad_arguments(fa):
     q, kc, vc, lens = _dev(*inputs.make_decode(2, 8, 2, 128, 256, 1, 256, seed=83))
     with pytest.raises(fa.FaError) as e:

@@ -75,6 +75,32 @@ def test_varlen_matches_oracle(fa, case):
         assert np.abs(lf[fin] - lse_ref[fin]).max() <= LSE_TOL
 
 
+def test_varlen_output_guard_bands(fa):
+    """Writes stay inside the packed O and LSE: sentinel pages around them are untouched,
+    with an empty sequence, a single row and a ragged tail in the batch."""
+    lens_q, lens_k, Hq, Hkv, D = [130, 0, 1, 257], [130, 7, 1, 300], 4, 2, 128
+    q, k, v, cq, ck = _packed(lens_q, lens_k, Hq, Hkv, D, seed=515)
+    dev = torch.device("cuda:0")
+    tq = sum(lens_q)
+    pad = 4096
+    o_buf = torch.full((pad + tq * Hq * D + pad,), 7.0, dtype=torch.bfloat16, device=dev)
+    l_buf = torch.full((pad + Hq * tq + pad,), 7.0, dtype=torch.float32, device=dev)
+    o = o_buf[pad:pad + tq * Hq * D].view(tq, Hq, D)
+    lse = l_buf[pad:pad + Hq * tq].view(Hq, tq)
+    fa.fa_fwd_varlen(q.to(dev), k.to(dev), v.to(dev), cq.to(dev), ck.to(dev), causal=True,
+                     out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(o_buf[:pad] == 7.0) and torch.all(o_buf[-pad:] == 7.0)
+    assert torch.all(l_buf[:pad] == 7.0) and torch.all(l_buf[-pad:] == 7.0)
+    o_ref, lse_ref = oracle.fwd_varlen(q, k, v, cq.numpy(), ck.numpy(), scale=1 / math.sqrt(D),
+                                       causal=True, window=(-1, -1))
+    fin = np.isfinite(lse_ref)
+    lf = lse.cpu().numpy()
+    assert np.array_equal(fin, np.isfinite(lf))
+    assert np.abs(o.float().cpu().numpy() - o_ref).max() <= O_TOL
+    assert np.abs(lf[fin] - lse_ref[fin]).max() <= LSE_TOL
+
+
 def test_varlen_equal_lengths_reproduce_fa_fwd_bitwise(fa):
     B, S, Hq, Hkv, D = 3, 333, 4, 2, 128
     g = torch.Generator().manual_seed(9)
