@@ -2,6 +2,7 @@
 profiling a single kernel (e.g. under ncu) on inputs resident on the GPU.
 
   python -m exact_tiled_attention_20_gb300.run_case fwd B S Hq Hkv D causal [iters]
+  python -m exact_tiled_attention_20_gb300.run_case fwd_window B S Hq Hkv D left right [iters]
   python -m exact_tiled_attention_20_gb300.run_case decode B Hq Hkv D Smax [iters]
   python -m exact_tiled_attention_20_gb300.run_case decode_workload [iters]
 
@@ -33,6 +34,15 @@ def main(argv):
         o = torch.empty_like(q)
         lse = torch.empty(B, Hq, S, device=dev, dtype=torch.float32)
         call = lambda: fa.fa_fwd(q, k, v, causal=bool(causal), out=o, lse=lse)  # noqa: E731
+    elif kind == "fwd_window":
+        B, S, Hq, Hkv, D, left, right = (int(x) for x in argv[1:8])
+        iters = int(argv[8]) if len(argv) > 8 else 3
+        q = torch.randn(B, S, Hq, D, device=dev, generator=g, dtype=torch.bfloat16)
+        k = torch.randn(B, S, Hkv, D, device=dev, generator=g, dtype=torch.bfloat16)
+        v = torch.randn(B, S, Hkv, D, device=dev, generator=g, dtype=torch.bfloat16)
+        o = torch.empty_like(q)
+        lse = torch.empty(B, Hq, S, device=dev, dtype=torch.float32)
+        call = lambda: fa.fa_fwd(q, k, v, window=(left, right), out=o, lse=lse)  # noqa: E731
     elif kind == "decode":
         B, Hq, Hkv, D, Smax = (int(x) for x in argv[1:6])
         iters = int(argv[6]) if len(argv) > 6 else 3
