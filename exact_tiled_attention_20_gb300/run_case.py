@@ -5,6 +5,7 @@ profiling a single kernel (e.g. under ncu) on inputs resident on the GPU.
   python -m exact_tiled_attention_20_gb300.run_case fwd_window B S Hq Hkv D left right [iters]
   python -m exact_tiled_attention_20_gb300.run_case decode B Hq Hkv D Smax [iters]
   python -m exact_tiled_attention_20_gb300.run_case decode_workload [iters]
+  python -m exact_tiled_attention_20_gb300.run_case decode_paged_workload [iters]
 
 Inputs are drawn on the device from a fixed seed (values do not matter for profiling);
 the script prints the mean time per call from CUDA events.
@@ -65,6 +66,24 @@ def main(argv):
         ws = torch.empty(fa.fa_decode_workspace_bytes(w.B, w.Hq, w.D, ns), dtype=torch.uint8, device=dev)
         o = torch.empty_like(q)
         call = lambda: fa.fa_decode_splitkv(q, kc, vc, lens, num_splits=ns, workspace=ws, out=o)  # noqa: E731
+    elif kind == "decode_paged_workload":
+        # the same workload in 256-key pages of a pool, the pages in a seeded random order
+        from . import inputs
+
+        w = inputs.DECODE
+        iters = int(argv[1]) if len(argv) > 1 else 3
+        q, kc, vc, lens = inputs.decode_inputs(w)
+        page = 256
+        mp = w.Smax // page
+        perm = torch.randperm(w.B * mp, generator=torch.Generator().manual_seed(7))
+        table = perm.view(w.B, mp).to(torch.int32)
+        kp = torch.empty((w.B * mp, page, w.Hkv, w.D), dtype=kc.dtype)
+        vp = torch.empty_like(kp)
+        kp[perm] = kc.view(w.B * mp, page, w.Hkv, w.D)
+        vp[perm] = vc.view(w.B * mp, page, w.Hkv, w.D)
+        q, kp, vp, table, lens = (t.to(dev) for t in (q, kp, vp, table, lens))
+        o = torch.empty_like(q)
+        call = lambda: fa.fa_decode_splitkv_paged(q, kp, vp, table, lens, out=o)  # noqa: E731
     else:
         raise SystemExit(__doc__)
     call()
