@@ -3,6 +3,7 @@ profiling a single kernel (e.g. under ncu) on inputs resident on the GPU.
 
   python -m exact_tiled_attention_20_gb300.run_case fwd B S Hq Hkv D causal [iters]
   python -m exact_tiled_attention_20_gb300.run_case fwd_window B S Hq Hkv D left right [iters]
+  python -m exact_tiled_attention_20_gb300.run_case fwd_varlen_workload [iters]
   python -m exact_tiled_attention_20_gb300.run_case decode B Hq Hkv D Smax [iters]
   python -m exact_tiled_attention_20_gb300.run_case decode_workload [iters]
   python -m exact_tiled_attention_20_gb300.run_case decode_paged_workload [iters]
@@ -44,6 +45,20 @@ def main(argv):
         o = torch.empty_like(q)
         lse = torch.empty(B, Hq, S, device=dev, dtype=torch.float32)
         call = lambda: fa.fa_fwd(q, k, v, window=(left, right), out=o, lse=lse)  # noqa: E731
+    elif kind == "fwd_varlen_workload":
+        # 16 causal sequences of U[256, 8192] rows (seed 1005), Hq = Hkv = 32, D = 128, packed
+        import numpy as np
+
+        iters = int(argv[1]) if len(argv) > 1 else 3
+        lens = [int(x) for x in np.random.default_rng(1005).integers(256, 8193, 16)]
+        tq = sum(lens)
+        q = torch.randn(tq, 32, 128, device=dev, generator=g, dtype=torch.bfloat16)
+        k = torch.randn(tq, 32, 128, device=dev, generator=g, dtype=torch.bfloat16)
+        v = torch.randn(tq, 32, 128, device=dev, generator=g, dtype=torch.bfloat16)
+        cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device=dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(32, tq, device=dev, dtype=torch.float32)
+        call = lambda: fa.fa_fwd_varlen(q, k, v, cu, cu, causal=True, out=o, lse=lse)  # noqa: E731
     elif kind == "decode":
         B, Hq, Hkv, D, Smax = (int(x) for x in argv[1:6])
         iters = int(argv[6]) if len(argv) > 6 else 3
