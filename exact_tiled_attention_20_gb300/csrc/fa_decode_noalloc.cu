@@ -53,7 +53,11 @@ fa_status fa_decode_splitkv_noalloc(const void* q, const void* k_cache, const vo
                                     const int32_t* kv_lens, void* o, float* lse, int B, int Hq,
                                     int Hkv, int D, int Smax, float scale, int num_splits,
                                     fa_dtype dtype, fa_stream_t stream) {
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Smax <= 0) return FA_ERR_INVALID_ARG;
+    // The same argument checks as fa_decode_splitkv come first, so an invalid or
+    // unsupported call returns the same status from either entry point.
+    const fa_status chk = fa::decode_check_args(q, k_cache, v_cache, kv_lens, o, lse, B, 1, Hq,
+                                                Hkv, D, Smax, scale, dtype);
+    if (chk != FA_OK) return chk;
     int ns = num_splits;
     if (ns <= 0) ns = fa_decode_default_splits(B, Hkv, Smax, 0);
     if (ns <= 0) return FA_ERR_CUDA;

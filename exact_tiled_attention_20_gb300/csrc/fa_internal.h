@@ -69,6 +69,12 @@ fa_status launch_fwd_d256(const FwdArgs& a, cudaStream_t s);
 
 fa_status launch_decode(const DecodeArgs& a, cudaStream_t s);
 
+// Argument checks shared by every decode entry point (pointers, alignment, sizes, dtype,
+// head dim, group size); FA_OK or the status the entry point returns.  Host only.
+fa_status decode_check_args(const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* kv_lens, const void* o, const float* lse, int B, int Sq,
+                            int Hq, int Hkv, int D, int Smax, float scale, fa_dtype dtype);
+
 // Sets the dynamic shared-memory limit of `func` once per device.
 bool ensure_smem_attr(const void* func, int bytes, int* done_flags);
 

@@ -109,3 +109,38 @@ def make_decode(B, Hq, Hkv, D, Smax, len_lo, len_hi, seed, amp=1.0, dtype="bf16"
     k = (torch.randn((B, Smax, Hkv, D), generator=g, dtype=torch.float32) * amp).to(dt)
     v = (torch.randn((B, Smax, Hkv, D), generator=g, dtype=torch.float32) * amp).to(dt)
     return q, k, v, lens
+
+
+# Inputs of the widened rows, measured beside the workloads above.
+WINDOW_LEFT = 1023  # sliding window: each query sees itself and the 1023 keys before it
+
+
+def varlen_lengths(n=16, lo=256, hi=8192, seed=1005):
+    """Sequence lengths of the variable-length batch: n draws from U[lo, hi] (numpy
+    generator ``default_rng(seed)``), packed in draw order."""
+    import numpy as np
+
+    return [int(x) for x in np.random.default_rng(seed).integers(lo, hi + 1, n)]
+
+
+def decode_multi_queries(w: DecodeWorkload, sq=4, seed=12):
+    """Query tokens [B, sq, Hq, D] for decoding several tokens over the cache of ``w``:
+    ``randn`` from ``Generator("cpu").manual_seed(seed)``, rounded to the workload dtype."""
+    g = torch.Generator("cpu").manual_seed(int(seed))
+    return (torch.randn((w.B, sq, w.Hq, w.D), generator=g, dtype=torch.float32) * w.amp).to(
+        _DTYPES[w.dtype])
+
+
+def paged_layout(k_cache, v_cache, page=256, seed=7):
+    """The same cache stored as a pool of ``page``-key pages in a seeded random order:
+    returns (k_pages, v_pages [B * Smax / page, page, Hkv, D], block_table int32
+    [B, Smax / page]) with page block_table[b][i] holding keys [i * page, (i + 1) * page)
+    of sequence b."""
+    B, smax, hkv, d = k_cache.shape
+    mp = smax // page
+    perm = torch.randperm(B * mp, generator=torch.Generator("cpu").manual_seed(int(seed)))
+    kp = torch.empty((B * mp, page, hkv, d), dtype=k_cache.dtype)
+    vp = torch.empty_like(kp)
+    kp[perm] = k_cache.reshape(B * mp, page, hkv, d)
+    vp[perm] = v_cache.reshape(B * mp, page, hkv, d)
+    return kp, vp, perm.view(B, mp).to(torch.int32)

@@ -119,3 +119,27 @@ def test_binding_rejects_cpu_tensors():
     q = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         fa.fa_fwd(q, q, q)
+
+
+def test_noalloc_decode_validates_like_the_workspace_decode(lib):
+    """fa_decode_splitkv_noalloc runs the same argument checks as fa_decode_splitkv before
+    it looks at its scratch: an invalid or unsupported call gets the same status."""
+    raw = ctypes.CDLL(lib[1])
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    raw.fa_decode_splitkv_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, I, I, P]
+    raw.fa_decode_splitkv_noalloc.restype = I
+    L = lib[0]
+    # (q, k, v, kv_lens, o, lse, B, Hq, Hkv, D, Smax, scale, num_splits)
+    base = [FAKE, FAKE, FAKE, FAKE, FAKE, None, 2, 8, 2, 128, 256, 0.1, 4]
+    cases = []
+    bad = list(base); bad[0] = None; cases.append((bad, 1))             # null q
+    bad = list(base); bad[3] = None; cases.append((bad, 1))             # null kv_lens
+    bad = list(base); bad[9] = 80; cases.append((bad, 2))               # head dim 80
+    bad = list(base); bad[7] = 3; cases.append((bad, 1))                # 8 heads over 3
+    bad = list(base); bad[7] = 64; bad[8] = 2; cases.append((bad, 2))   # group of 32 > 16
+    # an unsupported size whose partials would also overflow the scratch
+    bad = list(base); bad[9] = 4096; bad[12] = 4096; cases.append((bad, 2))
+    for args, code in cases:
+        assert raw.fa_decode_splitkv_noalloc(*args, 0, None) == code, args
+        ws = [FAKE, 1 << 30, 0, None]
+        assert L.fa_decode_splitkv(*args, *ws) == code, args

@@ -93,8 +93,50 @@ def test_clock_record_median_and_throttle_reasons(tmp_path):
     s.fh = open(s.path, "a")
     s.proc = _FakeProc()
     rec = s.stop()
-    assert rec == {"sm_mhz": 1980.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    # the three samples are all above the 300 W load threshold
+    assert rec == {"sm_mhz": 1980.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
+                   "samples": 3, "samples_under_load": 3, "power_cap_frac": round(2 / 3, 3),
+                   "power_w_max": 1395.0}
     assert not os.path.exists(s.path)
+
+
+def test_clock_record_keeps_only_samples_under_load():
+    lines = ["0, 1987, 2070, 150.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "0, 2070, 2070, 640.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "0, 2070, 2070, 650.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "0, 1987, 2070, [N/A], 0x0, Not Active, Not Active, Not Active, Not Active"]
+    rec = bench.parse_clock_csv(lines)
+    assert rec["sm_mhz"] == 2070.0 and rec["samples_under_load"] == 2 and rec["samples"] == 4
+    assert rec["power_cap_frac"] == 0.0 and rec["reasons"] == []
+    # with no sample under load, every sample counts
+    rec = bench.parse_clock_csv(lines[:1])
+    assert rec["sm_mhz"] == 1987.0 and rec["samples_under_load"] == 1
+
+
+def test_peak_follows_the_clock_record():
+    peaks = {"bf16_tflops": 1939.8, "bf16_tflops_sustained": 1703.7, "hbm_gbs": 6788.3}
+    burst = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "power_cap_frac": 0.1}
+    capped = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "power_cap_frac": 0.8}
+    slow = {"sm_mhz": 1485.0, "sm_max_mhz": 2070.0, "power_cap_frac": 0.0}
+    assert bench.choose_tensor_peak(peaks, "measured", burst)[0] == 1939.8
+    assert bench.choose_tensor_peak(peaks, "measured", capped)[0] == 1703.7
+    assert bench.choose_tensor_peak(peaks, "measured", slow)[0] == 1703.7
+    assert bench.choose_tensor_peak(peaks, "measured", None)[0] == 1703.7
+    r = bench.tensor_roofline(1637.0, peaks, "measured", burst, num_sms=152)
+    assert r["frac"] == round(1637.0 / 1939.8, 4) and "burst" in r["peak_kind"]
+    assert r["frac_of_sustained"] == round(1637.0 / 1703.7, 4)
+    nominal = 152 * 8192 * 2070e6 / 1e12
+    assert r["clock_nominal"]["peak"] == round(nominal, 1)
+
+
+def test_visible_keys_causal_and_window():
+    # bottom-right causal with Sq = 4, Sk = 6: row i sees i + 3 keys
+    assert [bench.visible_keys(i, 4, 6, True) for i in range(4)] == [3, 4, 5, 6]
+    assert [bench.visible_keys(i, 4, 6, False) for i in range(4)] == [6] * 4
+    # window (2, 0) with causal, Sq = Sk = 5: row i sees min(i + 1, 3) keys
+    assert [bench.visible_keys(i, 5, 5, True, (2, 0)) for i in range(5)] == [1, 2, 3, 3, 3]
+    # a row whose window lies before key 0 sees nothing (Sq > Sk, causal)
+    assert bench.visible_keys(0, 5, 2, True) == 0
 
 
 def test_clock_record_absent_without_nvidia_smi():

@@ -1,11 +1,11 @@
 """Full-size forward workloads on the GPU, checked against the oracle.
 
 Each workload runs at its full size through fa_fwd, exactly as the benchmark launches
-it (same inputs recipe, default scale, persistent grid).  The oracle computes a sample
-of output rows one by one: the corners of the first and last (batch, head), rows on
-both sides of the 128-row tile boundaries, and random rows.  Those rows must match
-within max|dO| <= 1e-2 and max|dLSE| <= 1e-3.  Every output row is also checked for
-properties that hold at any size:
+it (same inputs recipe, default scale, persistent grid).  The oracle computes whole
+heads -- every row of (b, h) = (0, 0), (B - 1, Hq - 1) and two seeded random heads --
+plus rows on both sides of the 128-row tile boundaries of a middle head and random rows
+anywhere; at S <= 1024 every row of every head.  Those rows must match within max|dO| <= 1e-2 and max|dLSE| <= 1e-3.  Every
+output row is also checked for properties that hold at any size:
   * O and LSE are finite;
   * each output is a convex combination of the visible V rows, so
     min_j V[j, d] <= O[i, d] <= max_j V[j, d] (up to bf16 rounding of O);
@@ -52,13 +52,32 @@ def _inputs(w):
     return _cache[key]
 
 
+def _heads(w, seed=0):
+    """(0, 0), (B - 1, Hq - 1) and two seeded random (b, h) pairs, all distinct."""
+    rng = np.random.default_rng(seed + w.seed)
+    heads = [(0, 0), (w.B - 1, w.Hq - 1)]
+    while len(heads) < 4:
+        bh = (int(rng.integers(w.B)), int(rng.integers(w.Hq)))
+        if bh not in heads:
+            heads.append(bh)
+    return heads
+
+
+FULL_CHECK_MAX_S = 1024  # at and below this length every row of every head is checked
+
+
 def _sample_rows(w, n_random=160, seed=0):
+    if w.Sq <= FULL_CHECK_MAX_S:
+        bb, hh, ii = np.meshgrid(np.arange(w.B), np.arange(w.Hq), np.arange(w.Sq), indexing="ij")
+        return np.stack([bb.ravel(), hh.ravel(), ii.ravel()], axis=1).astype(np.int64)
     rng = np.random.default_rng(seed)
     rows = set()
-    for b, h in ((0, 0), (w.B - 1, w.Hq - 1), (w.B // 2, w.Hq // 3)):
-        for i in (0, 1, 127, 128, 129, 255, 256, w.Sq // 2, w.Sq - 129, w.Sq - 128, w.Sq - 2, w.Sq - 1):
-            if 0 <= i < w.Sq:
-                rows.add((b, h, i))
+    for b, h in _heads(w, seed):
+        rows.update((b, h, i) for i in range(w.Sq))
+    b, h = w.B // 2, w.Hq // 3
+    for i in (0, 1, 127, 128, 129, 255, 256, w.Sq // 2, w.Sq - 129, w.Sq - 128, w.Sq - 2, w.Sq - 1):
+        if 0 <= i < w.Sq:
+            rows.add((b, h, i))
     for _ in range(n_random):
         rows.add((int(rng.integers(w.B)), int(rng.integers(w.Hq)), int(rng.integers(w.Sq))))
     return np.array(sorted(rows), dtype=np.int64)
@@ -103,11 +122,15 @@ def test_full_size_workload(fa, w):
     lse_s = lse[b, h, i].cpu().numpy()
     do = np.abs(o_s - o_ref).max()
     dl = np.abs(lse_s - lse_ref).max()
+    heads = _heads(w)
+    print(f"{w.name}: {len(rows)} rows checked, whole heads {heads}, "
+          f"max|dO| = {do:.3e}, max|dLSE| = {dl:.3e}")
+    assert len(rows) >= 4 * w.Sq
     assert do <= O_TOL, f"max|dO| = {do:.3e} over {len(rows)} rows"
     assert dl <= LSE_TOL, f"max|dLSE| = {dl:.3e} over {len(rows)} rows"
     # LSE >= max scaled score of the row
     hk = rows[:, 1] // g
-    for n in range(0, len(rows), 37):
+    for n in range(0, len(rows), max(37, len(rows) // 400)):
         bb, hh, ii = rows[n]
         kk = k[bb, :, hk[n]].double().numpy()
         s = w.scale * (kk @ q[bb, ii, hh].double().numpy())

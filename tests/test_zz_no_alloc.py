@@ -2,8 +2,9 @@
 device memory (a plugin inside a host runtime that owns all device allocations, or a
 serving loop that must never call cudaMalloc).  It keeps its scratch in a fixed array in
 the library's device image.  Called here through the C ABI; its output must match the
-regular fa_decode_splitkv (which takes a caller-allocated workspace) within the decode
-tolerances, on two calls in a row (the second reuses the scratch the first left behind).
+regular fa_decode_splitkv (which takes a caller-allocated workspace) and the CPU oracle's
+decode (the fp64 definition) within the decode tolerances, on two calls in a row (the
+second reuses the scratch the first left behind).
 
 This file is collected last so that a run stopping at the first failure has already run
 every other test.
@@ -11,9 +12,11 @@ every other test.
 import ctypes
 import math
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 from exact_tiled_attention_20_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -53,8 +56,9 @@ def test_noalloc_decode_matches_workspace_decode_twice(lib):
     dev = torch.device("cuda:0")
     cases = [(inputs.make_decode(4, 32, 8, 128, 4096, 100, 4096, seed=91), 0),
              (inputs.make_decode(3, 16, 2, 128, 2500, 1, 2500, seed=92), 7)]
-    for (q, kc, vc, lens), ns in cases:
-        q, kc, vc, lens = (t.to(dev) for t in (q, kc, vc, lens))
+    for (qh, kh, vh, lh), ns in cases:
+        o_def, lse_def = oracle.decode(qh, kh, vh, lh, scale=1.0 / math.sqrt(qh.shape[-1]))
+        q, kc, vc, lens = (t.to(dev) for t in (qh, kh, vh, lh))
         o_ref, lse_ref = fa.fa_decode_splitkv(q, kc, vc, lens, num_splits=ns)
         for _ in range(2):
             o = torch.full_like(q, float("nan"))
@@ -63,6 +67,9 @@ def test_noalloc_decode_matches_workspace_decode_twice(lib):
             torch.cuda.synchronize()
             assert (o.float() - o_ref.float()).abs().max().item() <= O_TOL
             assert (lse - lse_ref).abs().max().item() <= LSE_TOL
+            o_np = o.float().cpu().numpy()[:, 0]
+            assert np.abs(o_np - o_def).max() <= O_TOL
+            assert np.abs(lse.cpu().numpy() - lse_def).max() <= LSE_TOL
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
