@@ -852,6 +852,28 @@ def sweep_configs(args, fa, device, peaks, peak_src, num_sms):
     del kp_d, vp_d, tb_d, kp, vp, q_d, l_d, o_d, lse_d, ws
     torch.cuda.empty_cache()
 
+    # -- the decode workload's shape and lengths at the other head dims
+    for wdd in inputs.DECODE_D_SWEEP:
+        dq, dk, dv, dl = inputs.decode_inputs(wdd)
+        lens_l = dl.tolist()
+        ns = fa.fa_decode_default_splits(wdd.B, wdd.Hkv, wdd.Smax)
+        q_d, k_d, v_d, l_d = (t.to(device) for t in (dq, dk, dv, dl))
+        ws = torch.empty(fa.fa_decode_workspace_bytes(wdd.B, wdd.Hq, wdd.D, ns), dtype=torch.uint8,
+                         device=device)
+        o_d = torch.empty_like(q_d)
+        lse_d = torch.empty((wdd.B, wdd.Hq), dtype=torch.float32, device=device)
+        e, gbs = dec_entry(
+            f"decode_d{wdd.D}", "fa_decode_splitkv",
+            lambda: fa.fa_decode_splitkv(q_d, k_d, v_d, l_d, scale=wdd.scale, num_splits=ns,
+                                         workspace=ws, out=o_d, lse=lse_d),
+            o_d, lse_d, lambda: oracle.decode(dq, dk, dv, lens_l, scale=wdd.scale, nthreads=cores),
+            decode_bytes(wdd, lens_l),
+            f"B=8, Hq=32, Hkv=8, D={wdd.D}, the decode workload's lengths, Smax=32768, "
+            f"num_splits={ns}")
+        out.append((e, "hbm", gbs))
+        del q_d, k_d, v_d, l_d, ws, o_d, lse_d, dq, dk, dv
+        torch.cuda.empty_cache()
+
     clocks = sampler.stop()
     if fa.fa_last_device_status() != 0:
         raise RuntimeError("device status reported a kernel timeout during the per-workload runs")

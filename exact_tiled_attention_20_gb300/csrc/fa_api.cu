@@ -208,7 +208,7 @@ fa_status decode_check_args(const void* q, const void* k_cache, const void* v_ca
     if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
     if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_UNSUPPORTED;
-    if (D != 128) return FA_ERR_UNSUPPORTED;
+    if (D != 64 && D != 96 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
     if (Sq <= 0) return FA_ERR_INVALID_ARG;
     if ((Hq / Hkv) * Sq > 16 || B > 1024) return FA_ERR_UNSUPPORTED;
     if ((long long)B * Smax > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;

@@ -1,759 +1,17 @@
-// fa_decode.cu -- split-KV (Flash-Decoding) single-token attention for sm_103a.
-//
-// What is computed: for each sequence b and query head h, the attention of the single
-// query q[b, h] over the cached keys/values [0, kv_lens[b]) of K/V head h / (Hq / Hkv)
-// (page "flash-attention-v100", flash_attn_with_kvcache with cache_seqlens; "Changelog",
-// "2.2: Optimize for inference").  As the Flash-Decoding steps describe (page
-// "flash attention-2 github"): (1) the keys are cut into chunks, (2) each chunk's attention
-// is computed independently, writing a partial output and its log-sum-exp, (3) a separate
-// kernel merges them with the log-sum-exp weights.
-//
-// Splitting (the reading of "split the loading across thread blocks" taken here): the
-// keys of every (sequence b, kv head) pair, in 128-key tiles, are laid end to end in the
-// order (b, kv head), and CTA c takes the tiles [c W, (c + 1) W).  W is the total divided
-// by the grid, so every CTA streams the same number of tiles whatever the length mix,
-// but at least ceil(T_max / (num_splits - 1)) for the longest pair's T_max tiles, so no
-// pair meets more than num_splits ranges.  A pair cut by range boundaries yields one
-// segment per range it meets; each segment is computed independently and writes a
-// partial output and its log-sum-exp into the pair's next slot, which the merge kernel
-// combines.
-//
-// Split kernel (persistent, one CTA per SM, walking the work items):
-//  * the producer warp streams, per item, the Q rows of the query heads sharing the KV head
-//    (a 16-row box) and the item's K/V tiles of 128 keys through a 3-stage TMA ring;
-//  * the MMA warp computes S^T = K Q^T with the 128 keys of a tile as the M dimension and
-//    the query heads (padded to 16) as N, into TMEM, then O^T += V^T P^T with the 128 head
-//    dims as M (V read MN-major straight from the swizzled tile, P^T from shared memory);
-//  * four compute warps own one key (for S^T) and one head dim (for O^T) each: per tile a
-//    cross-warp max per head, exp2 with the scale folded in, a lazily rescaled O^T, and at
-//    the end of an item the division by l and the partial (o, lse) store.
-// Decode reads every K/V byte exactly once: HBM bandwidth is the roofline.
-#include <cuda.h>
-#include <cuda_runtime.h>
-
-#include <cstdint>
-
+// fa_decode.cu -- head-dim dispatch of the split-KV decode (kernels in fa_decode.cuh, one
+// instantiation per head dim in fa_decode_d{64,96,128,256}.cu, compiled in parallel).
 #include "fa_internal.h"
-#include "fa_ptx.cuh"
 
 namespace fa {
 
-struct DecParams {
-    int B, Hq, Hkv, group, Smax, ns;
-    float scale_log2;
-    const int32_t* kv_lens;
-    float* o_part;    // [B, Hq, ns, D]
-    float* lse_part;  // [B, Hq, ns]
-    int split_grid;   // CTAs of the split kernel (sets the range width)
-    void* o;          // [B, Hq, D]
-    float* lse;       // [B, Hq] or null
-    int q_rows;  // query-head rows per Q box; rows past q_rows * sq are never read
-    // Several query tokens per sequence (flash_attn_with_kvcache with seqlen_q > 1): the
-    // MMA's N columns hold (token s, head h) as column s * group + h; with `causal` token s
-    // sees keys j <= kv_len - sq + s (bottom-right alignment).  sq = 1 for plain decode.
-    int sq, causal;
-    // Paged cache (page "flash-attention-v100", flash_attn_with_kvcache block_table;
-    // "Changelog", "2.5: Paged KV cache"): key r of sequence b is row r % page_size of
-    // page block_table[b * max_pages + r / page_size]; page_size is a multiple of 128.
-    const int32_t* block_table;  // null: contiguous [B, Smax, Hkv, D] cache
-    int page_size, max_pages;
-    int* status;
-};
-
-constexpr int kDecD = 128;
-constexpr int kDecBN = 128;  // keys per tile = MMA M
-constexpr int kDecNS = 3;
-constexpr int kDecDA = kDecD / 64;
-constexpr int kDecKVBytes = kDecBN * kDecDA * 128;  // 32 KB
-constexpr int kDecQBytes = kDecDA * 16 * 128;       // 4 KB
-constexpr int kDecPBytes = (kDecBN / 64) * 16 * 128;  // 4 KB
-constexpr int kDecMaxB = 1024;
-constexpr int kDecThreads = 192;
-constexpr int kDecProducerWarp = 4;
-constexpr int kDecMmaWarp = 5;
-constexpr int kDecTmemCols = 64;  // S^T slots at 0 and 16, O^T at 32
-
-// barrier indices
-constexpr int kDBarQFull = 0;                   // 2
-constexpr int kDBarQEmpty = kDBarQFull + 2;     // 2
-constexpr int kDBarKFull = kDBarQEmpty + 2;     // NS
-constexpr int kDBarKEmpty = kDBarKFull + kDecNS;
-constexpr int kDBarVFull = kDBarKEmpty + kDecNS;
-constexpr int kDBarVEmpty = kDBarVFull + kDecNS;
-constexpr int kDBarSFull = kDBarVEmpty + kDecNS;  // 2
-// P full and O done: one barrier per P^T buffer.  With P^T double-buffered the compute
-// warps may finish tile j + 1 before the MMA warp has observed tile j; a single barrier
-// would then complete two phases ahead of its waiter and the parity wait would miss one.
-constexpr int kDBarPFull = kDBarSFull + 2;       // 2
-constexpr int kDBarODone = kDBarPFull + 2;       // 2
-constexpr int kDBarODrained = kDBarODone + 2;
-constexpr int kDBarFinal = kDBarODrained + 1;
-constexpr int kDNumBars = kDBarFinal + 1;
-
-struct DecSmemTail {
-    uint64_t bars[kDNumBars];
-    alignas(16) float red[2][4][16];   // per-tile cross-warp max, double-buffered
-    alignas(16) float lred[4][16];     // end-of-item cross-warp sums
-    int lens[kDecMaxB];
-    int prefix[kDecMaxB + 1];  // exclusive prefix over b of the tiles of one pair of b
-    int warp_sums[4];
-    int max_len;
-    int width;        // W, tiles per CTA range
-    int total_tiles;  // Hkv * prefix[B]
-    uint32_t tmem_slot;
-    int abort_flag;
-};
-
-// P^T is double-buffered: the compute warps write tile j's while P.V of tile j-1 reads
-// the other buffer.
-constexpr int kDecTileBytes = 2 * kDecNS * kDecKVBytes + 2 * kDecQBytes + 2 * kDecPBytes;
-constexpr int kDecSmemBytes = 1024 + kDecTileBytes + (int)sizeof(DecSmemTail);
-static_assert(kDecSmemBytes <= 232448, "decode shared memory budget");
-
-// One segment of work: keys [k0, k1) of pair (b, hk), written to partial slot c.
-struct DecItem {
-    int b, hk, c, k0, k1, ntiles;
-};
-
-// Width W of the CTA ranges (shared by the split and merge kernels, which must agree).
-__device__ __forceinline__ int decode_range_width(int total_tiles, int max_pair_tiles, int grid, int ns) {
-    long long w = ((long long)total_tiles + grid - 1) / grid;
-    if (ns >= 2)
-        w = max(w, ((long long)max_pair_tiles + ns - 2) / (ns - 1));
-    else
-        w = max(w, (long long)total_tiles);  // one range: no pair is cut
-    return (int)max(w, 1LL);
-}
-
-// The next segment of this CTA's range, starting at tile x (x advances past it).
-__device__ __forceinline__ bool next_segment(const DecSmemTail& t, int B, int Hkv, int& x, int end,
-                                             DecItem& it) {
-    if (x >= end) return false;
-    int lo = 0, hi = B;  // largest b with Hkv * prefix[b] <= x; that b has tiles
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (Hkv * t.prefix[mid] <= x) lo = mid; else hi = mid;
-    }
-    const int tb = t.prefix[lo + 1] - t.prefix[lo];
-    const int hk = (x - Hkv * t.prefix[lo]) / tb;
-    const int pstart = Hkv * t.prefix[lo] + hk * tb;  // first tile of pair (lo, hk)
-    const int seg_end = min(end, pstart + tb);
-    it.b = lo;
-    it.hk = hk;
-    it.c = (int)blockIdx.x - pstart / t.width;  // ranges met by this pair before this one
-    it.k0 = (x - pstart) * kDecBN;
-    it.k1 = min((seg_end - pstart) * kDecBN, t.lens[lo]);
-    it.ntiles = seg_end - x;
-    x = seg_end;
-    return true;
-}
-
-// Shared-memory byte address of P^T[h][key] in the 128-byte-swizzled K-major layout of a
-// 16-row x 128-key operand (two 64-key atoms of 16 rows x 128 bytes).
-__device__ __forceinline__ uint32_t pt_addr(uint32_t sP, int h, int key) {
-    const uint32_t byte = (uint32_t)(key & 63) * 2u;
-    return sP + (uint32_t)(key >> 6) * 2048u + (uint32_t)h * 128u +
-           ((((byte >> 4) ^ (uint32_t)(h & 7)) << 4) | (byte & 15u));
-}
-
-__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
-    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// Per-column reduction over the 32 lanes of a warp for N = 4, 8 or 16 columns: each of
-// the first log2(N) butterfly steps halves the columns a lane carries (it keeps one half
-// and trades the other with its partner), the remaining steps combine plain values.
-// Afterwards lane l holds the result for column reduce_col<N>(l).  N - 1 + 5 - log2(N)
-// shuffles instead of 5 N.
-template <int N>
-__device__ __forceinline__ int reduce_col(int lane) {
-    int col = 0, n = N, m = 16;
-#pragma unroll
-    for (; n > 1; n >>= 1, m >>= 1)
-        if (lane & m) col += n / 2;
-    return col;
-}
-
-template <int N, bool kMax>
-__device__ __forceinline__ float warp_reduce_cols(float (&v)[N], int lane) {
-    int m = 16;
-#pragma unroll
-    for (int n = N; n > 1; n >>= 1, m >>= 1) {
-        const bool up = (lane & m) != 0;
-#pragma unroll
-        for (int i = 0; i < n / 2; ++i) {
-            const float send = up ? v[i] : v[i + n / 2];
-            const float keep = up ? v[i + n / 2] : v[i];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, m);
-            v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
-        }
-    }
-    float r = v[0];
-#pragma unroll
-    for (; m > 0; m >>= 1) {
-        const float o = __shfl_xor_sync(0xffffffffu, r, m);
-        r = kMax ? fmaxf(r, o) : r + o;
-    }
-    return r;
-}
-
-template <bool kBF16>
-__device__ __forceinline__ uint16_t to16(float x) {
-    uint32_t w = pack2<kBF16>(x, 0.f);
-    return (uint16_t)(w & 0xffffu);
-}
-
-template <int GMAX, bool kBF16>
-__global__ void __launch_bounds__(kDecThreads, 1)
-    fa_decode_split_kernel(const __grid_constant__ CUtensorMap tm_q,
-                           const __grid_constant__ CUtensorMap tm_k,
-                           const __grid_constant__ CUtensorMap tm_v, const DecParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_u32 = smem_u32(smem_raw);
-    const uint32_t base = (raw_u32 + 1023u) & ~1023u;
-    uint8_t* base_gen = smem_raw + (base - raw_u32);
-    const uint32_t sK = base;
-    const uint32_t sV = sK + kDecNS * kDecKVBytes;
-    const uint32_t sQ = sV + kDecNS * kDecKVBytes;
-    const uint32_t sP = sQ + 2 * kDecQBytes;
-    DecSmemTail& T = *reinterpret_cast<DecSmemTail*>(base_gen + kDecTileBytes);
-    auto bar = [&](int i) -> uint32_t { return smem_u32(&T.bars[i]); };
-
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int lane = tid & 31;
-    const WaitCtx wc{&T.abort_flag, p.status};
-
-    // ---- setup: barriers, TMEM, and the work-item table from kv_lens
-    if (tid == 0) {
-        for (int i = 0; i < kDNumBars; ++i)
-            mbar_init(bar(i), (i == kDBarPFull || i == kDBarPFull + 1 || i == kDBarODrained) ? 128u : 1u);
-        T.abort_flag = 0;
-        T.max_len = 0;
-        fence_mbar_init();
-    }
-    if (warp == kDecMmaWarp) {
-        tmem_alloc(smem_u32(&T.tmem_slot), kDecTmemCols);
-        tmem_relinquish();
-    }
-    if (warp == kDecProducerWarp && lane == 0) {
-        prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_k);
-        prefetch_tmap(&tm_v);
-    }
-    // P^T rows past the group stay zero for the whole kernel.
-    for (int i = tid; i < 2 * kDecPBytes / 4; i += kDecThreads)
-        reinterpret_cast<uint32_t*>(base_gen + (sP - base))[i] = 0u;
-    fence_proxy_async_smem();
-    __syncthreads();
-    for (int b = tid; b < p.B; b += kDecThreads) {
-        const int len = min(max(p.kv_lens[b], 0), p.Smax);
-        T.lens[b] = len;
-        atomicMax(&T.max_len, len);
-    }
-    __syncthreads();
-    {
-        // exclusive scan over b of the tiles of one pair, 128 threads x up to 8 entries each
-        const int per_t = (p.B + 127) / 128;
-        int local = 0;
-        if (tid < 128) {
-            for (int i = 0; i < per_t; ++i) {
-                const int b = tid * per_t + i;
-                if (b < p.B) local += (T.lens[b] + kDecBN - 1) / kDecBN;
-            }
-        }
-        int incl = local;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        if (tid < 128 && lane == 31) T.warp_sums[warp] = incl;
-        __syncthreads();
-        if (tid < 128) {
-            int run = incl - local;
-            for (int w = 0; w < warp; ++w) run += T.warp_sums[w];
-            for (int i = 0; i < per_t; ++i) {
-                const int b = tid * per_t + i;
-                if (b < p.B) {
-                    T.prefix[b] = run;
-                    run += (T.lens[b] + kDecBN - 1) / kDecBN;
-                }
-            }
-            if (tid == 127) T.prefix[p.B] = run;
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {
-        T.total_tiles = p.Hkv * T.prefix[p.B];
-        T.width = decode_range_width(T.total_tiles, (T.max_len + kDecBN - 1) / kDecBN, (int)gridDim.x, p.ns);
-    }
-    __syncthreads();
-    const uint32_t tmem = T.tmem_slot;
-    // This CTA's range of tiles.
-    const int x0 = (int)min((long long)blockIdx.x * T.width, (long long)T.total_tiles);
-    const int x_end = min(x0 + T.width, T.total_tiles);
-    // The merge kernel may be scheduled now; it waits for this grid's results itself.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-    if (warp == kDecProducerWarp) {
-        // -------------------------------------------------------------- producer ----
-        if (lane == 0) {
-            uint32_t kv_it = 0, icount = 0;
-            bool ok = true;
-            // Every K/V row is read exactly once by this kernel.
-            const uint64_t kv_policy = l2_policy_evict_first();
-            int x = x0;
-            DecItem it;
-            while (ok && next_segment(T, p.B, p.Hkv, x, x_end, it)) {
-                const uint32_t qs = icount & 1u;
-                ok = mbar_wait(bar(kDBarQEmpty + qs), ((icount >> 1) & 1u) ^ 1u, wc);
-                if (!ok) break;
-                mbar_arrive_expect_tx(bar(kDBarQFull + qs), kDecDA * p.q_rows * p.sq * 128);
-                for (int a = 0; a < kDecDA; ++a)
-                    tma_load_4d(sQ + qs * kDecQBytes + a * 2048, &tm_q, bar(kDBarQFull + qs), a * 64,
-                                it.hk * p.group, 0, it.b);
-                // Paged caches: the page of the next tile is fetched while this one waits.
-                auto page_of = [&](int r) -> int {
-                    return p.block_table[(size_t)it.b * p.max_pages + r / p.page_size];
-                };
-                int next_page = (p.block_table && it.ntiles > 0) ? page_of(it.k0) : 0;
-                for (int j = 0; j < it.ntiles && ok; ++j) {
-                    const uint32_t st = kv_it % kDecNS;
-                    const uint32_t ph = ((kv_it / kDecNS) & 1u) ^ 1u;
-                    const int row = it.k0 + j * kDecBN;
-                    int c2 = row, c3 = it.b;  // contiguous: (key row, sequence)
-                    if (p.block_table) {      // paged: (row within page, page)
-                        c2 = row % p.page_size;
-                        c3 = next_page;
-                        if (j + 1 < it.ntiles) next_page = page_of(row + kDecBN);
-                    }
-                    ok = mbar_wait(bar(kDBarKEmpty + st), ph, wc);
-                    if (!ok) break;
-                    mbar_arrive_expect_tx(bar(kDBarKFull + st), kDecKVBytes);
-                    for (int a = 0; a < kDecDA; ++a)
-                        tma_load_4d_hint(sK + st * kDecKVBytes + a * (kDecBN * 128), &tm_k,
-                                         bar(kDBarKFull + st), a * 64, it.hk, c2, c3, kv_policy);
-                    ok = mbar_wait(bar(kDBarVEmpty + st), ph, wc);
-                    if (!ok) {
-                        mbar_wait_drain(bar(kDBarKFull + st), (kv_it / kDecNS) & 1u);
-                        break;
-                    }
-                    mbar_arrive_expect_tx(bar(kDBarVFull + st), kDecKVBytes);
-                    for (int a = 0; a < kDecDA; ++a)
-                        tma_load_4d_hint(sV + st * kDecKVBytes + a * (kDecBN * 128), &tm_v,
-                                         bar(kDBarVFull + st), a * 64, it.hk, c2, c3, kv_policy);
-                    ++kv_it;
-                }
-                ++icount;
-            }
-            for (uint32_t d = 0; d < (uint32_t)kDecNS && d < kv_it; ++d) {
-                const uint32_t last = kv_it - 1 - d;
-                mbar_wait_drain(bar(kDBarKFull + last % kDecNS), (last / kDecNS) & 1u);
-                mbar_wait_drain(bar(kDBarVFull + last % kDecNS), (last / kDecNS) & 1u);
-            }
-            for (uint32_t d = 0; d < 2u && d < icount; ++d) {
-                const uint32_t last = icount - 1 - d;
-                mbar_wait_drain(bar(kDBarQFull + (last & 1u)), (last >> 1) & 1u);
-            }
-        }
-        __syncwarp();
-    } else if (warp == kDecMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer ----
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = make_idesc_f16(128, 16, kBF16, false, false);
-            constexpr uint32_t idesc_o = make_idesc_f16(128, 16, kBF16, true, false);
-            uint32_t kv_it = 0, icount = 0, it_s = 0;
-            bool ok = true;
-            const uint64_t dk0 = make_sdesc_sw128(sK, 16, 1024);
-            const uint64_t dq0 = make_sdesc_sw128(sQ, 16, 1024);
-            const uint64_t dv0 = make_sdesc_sw128(sV, kDecBN * 128, 1024);
-            const uint64_t dp0 = make_sdesc_sw128(sP, 16, 1024);
-            auto issue_s = [&](uint32_t qs, uint32_t kst, uint32_t slot) {
-                const uint64_t a = dk0 + (uint64_t)((kst * kDecKVBytes) >> 4);
-                const uint64_t b = dq0 + (uint64_t)((qs * kDecQBytes) >> 4);
-                const uint32_t d = tmem + slot * 16;
-                umma_ss_imm<false>(d, a, b, idesc_s);
-#pragma unroll
-                for (int kk = 1; kk < kDecD / 16; ++kk)
-                    umma_ss_imm<true>(d, a + (uint64_t)(((kk >> 2) * (kDecBN * 128) + (kk & 3) * 32) >> 4),
-                                      b + (uint64_t)(((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), idesc_s);
-            };
-            auto issue_pv = [&](uint32_t vst, uint32_t pbuf, bool acc) {
-                const uint64_t a = dv0 + (uint64_t)((vst * kDecKVBytes) >> 4);
-                const uint64_t b = dp0 + (uint64_t)((pbuf * kDecPBytes) >> 4);
-                if (acc)
-                    umma_ss_imm<true>(tmem + 32, a, b, idesc_o);
-                else
-                    umma_ss_imm<false>(tmem + 32, a, b, idesc_o);
-#pragma unroll
-                for (int kk = 1; kk < kDecBN / 16; ++kk)
-                    umma_ss_imm<true>(tmem + 32, a + (uint64_t)((kk * (16 * 128)) >> 4),
-                                      b + (uint64_t)(((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), idesc_o);
-            };
-            int x = x0;
-            DecItem item;
-            while (ok && next_segment(T, p.B, p.Hkv, x, x_end, item)) {
-                const int n = item.ntiles;
-                const uint32_t qs = icount & 1u;
-                ok = mbar_wait(bar(kDBarQFull + qs), (icount >> 1) & 1u, wc);
-                if (!ok) break;
-                {
-                    const uint32_t st = kv_it % kDecNS;
-                    ok = mbar_wait(bar(kDBarKFull + st), (kv_it / kDecNS) & 1u, wc);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s(qs, st, it_s & 1u);
-                    umma_commit(bar(kDBarSFull + (it_s & 1u)));
-                    umma_commit(bar(kDBarKEmpty + st));
-                    if (n == 1) umma_commit(bar(kDBarQEmpty + qs));
-                }
-                for (int j = 0; j < n && ok; ++j) {
-                    const uint32_t cur = kv_it + j;
-                    const uint32_t st = cur % kDecNS;
-                    if (j + 1 < n) {
-                        const uint32_t nst = (cur + 1) % kDecNS;
-                        ok = mbar_wait(bar(kDBarKFull + nst), ((cur + 1) / kDecNS) & 1u, wc);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_s(qs, nst, (it_s + 1) & 1u);
-                        umma_commit(bar(kDBarSFull + ((it_s + 1) & 1u)));
-                        umma_commit(bar(kDBarKEmpty + nst));
-                        if (j + 2 == n) umma_commit(bar(kDBarQEmpty + qs));
-                    }
-                    ok = mbar_wait(bar(kDBarPFull + (it_s & 1u)), (it_s >> 1) & 1u, wc);
-                    if (ok && j == 0 && icount > 0)
-                        ok = mbar_wait(bar(kDBarODrained), (icount - 1) & 1u, wc);
-                    if (ok) ok = mbar_wait(bar(kDBarVFull + st), (cur / kDecNS) & 1u, wc);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(st, it_s & 1u, j > 0);
-                    umma_commit(bar(kDBarODone + (it_s & 1u)));
-                    umma_commit(bar(kDBarVEmpty + st));
-                    ++it_s;
-                }
-                kv_it += n;
-                ++icount;
-            }
-            umma_commit(bar(kDBarFinal));
-            mbar_wait_drain(bar(kDBarFinal), 0);
-        }
-        __syncwarp();
-    } else {
-        // --------------------------------------------------------- compute warps ----
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-        const float kNegInf = -__int_as_float(0x7f800000);
-        const int g = p.group;
-        uint32_t it_s = 0;
-        bool ok = true;
-        int x = x0;
-        DecItem item;
-        while (ok && next_segment(T, p.B, p.Hkv, x, x_end, item)) {
-            float m_run[GMAX], l_part[GMAX];
-#pragma unroll
-            for (int h = 0; h < GMAX; ++h) {
-                m_run[h] = kNegInf;
-                l_part[h] = 0.f;
-            }
-            for (int j = 0; j < item.ntiles; ++j) {
-                const uint32_t slot = it_s & 1u;
-                ok = mbar_wait(bar(kDBarSFull + slot), (it_s >> 1) & 1u, wc);
-                if (!ok) break;
-                tc_fence_after();
-                uint32_t u[16];
-                tmem_ld_32x32b_x16(lane_base + slot * 16, u);
-                tmem_wait_ld(u);
-                const int key = item.k0 + j * kDecBN + tid;
-                const int ncols = g * p.sq;
-                // Token s sees keys <= len - sq + s; column h holds token h / g, so with
-                // causal tokens this key is visible to columns h >= (key - len + sq) * g.
-                const int lim0 = T.lens[item.b] - p.sq;
-                const int h_lo = p.causal ? max(key - lim0, 0) * g : 0;
-                const int h_hi = key < item.k1 ? ncols : 0;  // columns [h_lo, h_hi) see it
-                float sv[GMAX], mx[GMAX];
-#pragma unroll
-                for (int h = 0; h < GMAX; ++h) {
-                    const bool vis = h >= h_lo && h < h_hi;
-                    sv[h] = vis ? __uint_as_float(u[h]) : kNegInf;
-                    mx[h] = sv[h];
-                }
-                // per-column max over this warp's 32 keys, then over the four warps
-                const float wm = warp_reduce_cols<GMAX, true>(mx, lane);
-                if ((lane & (32 / GMAX - 1)) == 0) T.red[j & 1][warp][reduce_col<GMAX>(lane)] = wm;
-                named_bar_sync(1, 128);
-                float mb4[GMAX];
-#pragma unroll
-                for (int h4 = 0; h4 < GMAX; h4 += 4) {
-                    float4 r[4];
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) r[w] = *reinterpret_cast<const float4*>(&T.red[j & 1][w][h4]);
-                    mb4[h4 + 0] = fmaxf(fmaxf(r[0].x, r[1].x), fmaxf(r[2].x, r[3].x));
-                    mb4[h4 + 1] = fmaxf(fmaxf(r[0].y, r[1].y), fmaxf(r[2].y, r[3].y));
-                    mb4[h4 + 2] = fmaxf(fmaxf(r[0].z, r[1].z), fmaxf(r[2].z, r[3].z));
-                    mb4[h4 + 3] = fmaxf(fmaxf(r[0].w, r[1].w), fmaxf(r[2].w, r[3].w));
-                }
-                float alpha[GMAX], msub[GMAX];
-                bool any_rescale = false;
-#pragma unroll
-                for (int h = 0; h < GMAX; ++h) {
-                    const float mb = mb4[h] * p.scale_log2;
-                    const bool bump = mb > m_run[h] + 8.0f;
-                    const float mn = bump ? mb : m_run[h];
-                    alpha[h] = bump ? ex2_approx(m_run[h] - mn) : 1.0f;
-                    any_rescale |= bump;
-                    m_run[h] = mn;
-                    msub[h] = (mn == kNegInf) ? 0.f : mn;
-                }
-                float pv[GMAX];
-#pragma unroll
-                for (int h = 0; h < GMAX; ++h) {
-                    pv[h] = ex2_approx(fmaf(sv[h], p.scale_log2, -msub[h]));
-                    l_part[h] = l_part[h] * alpha[h] + pv[h];
-                }
-                // This tile's P^T buffer was last read by the P.V of tile it_s - 2.
-                if (it_s >= 2) {
-                    ok = mbar_wait(bar(kDBarODone + (it_s & 1u)), ((it_s - 2) >> 1) & 1u, wc);
-                    if (!ok) break;
-                }
-                if (j > 0 && any_rescale) {  // uniform: every thread saw the same maxima
-                    // the previous P.V must have finished accumulating into O
-                    ok = mbar_wait(bar(kDBarODone + ((it_s - 1) & 1u)), ((it_s - 1) >> 1) & 1u, wc);
-                    if (!ok) break;
-                    tc_fence_after();
-                    uint32_t ov[16];
-                    tmem_ld_32x32b_x16(lane_base + 32, ov);
-                    tmem_wait_ld(ov);
-#pragma unroll
-                    for (int h = 0; h < GMAX; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
-                    tmem_st_32x32b_x16(lane_base + 32, ov);
-                    tmem_wait_st();
-                }
-                const uint32_t sPb = sP + (it_s & 1u) * kDecPBytes;
-#pragma unroll
-                for (int h = 0; h < GMAX; ++h) st_shared_u16(pt_addr(sPb, h, tid), to16<kBF16>(pv[h]));
-                fence_proxy_async_smem();
-                tc_fence_before();
-                mbar_arrive(bar(kDBarPFull + (it_s & 1u)));
-                ++it_s;
-            }
-            if (!ok) break;
-            // ---- end of item: O^T / l -> partial output, log-sum-exp per head
-            ok = mbar_wait(bar(kDBarODone + ((it_s - 1) & 1u)), ((it_s - 1) >> 1) & 1u, wc);
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t ov[16];
-            tmem_ld_32x32b_x16(lane_base + 32, ov);
-            tmem_wait_ld(ov);
-            tc_fence_before();
-            mbar_arrive(bar(kDBarODrained));
-            {
-                float ls[GMAX];
-#pragma unroll
-                for (int h = 0; h < GMAX; ++h) ls[h] = l_part[h];
-                const float wl = warp_reduce_cols<GMAX, false>(ls, lane);
-                if ((lane & (32 / GMAX - 1)) == 0) T.lred[warp][reduce_col<GMAX>(lane)] = wl;
-            }
-            named_bar_sync(1, 128);
-#pragma unroll
-            for (int h = 0; h < GMAX; ++h) {
-                const float lt = (T.lred[0][h] + T.lred[1][h]) + (T.lred[2][h] + T.lred[3][h]);
-                if (h < g * p.sq) {
-                    // column h is (token h / g, head hk * g + h % g); rows are [B, sq, Hq]
-                    const size_t qrow = ((size_t)item.b * p.sq + h / g) * p.Hq + (size_t)item.hk * g + h % g;
-                    const size_t row = qrow * p.ns + item.c;
-                    p.o_part[row * kDecD + tid] = lt > 0.f ? __uint_as_float(ov[h]) / lt : 0.f;
-                    if (tid == 0)
-                        p.lse_part[row] =
-                            lt > 0.f ? (m_run[h] + lg2_approx(lt)) * 0.69314718055994531f : kNegInf;
-                }
-            }
-            // lred is rewritten only after the next item's per-tile barriers
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    if (warp == kDecMmaWarp) {
-        tc_fence_after();
-        tmem_dealloc(tmem, kDecTmemCols);
-    }
-}
-
-// Merge kernel: one warp per (b, query head); lane l owns head dims 4l .. 4l+3.
-template <bool kBF16>
-__global__ void __launch_bounds__(128)
-    fa_decode_combine_kernel(const DecParams p) {
-    // The split kernel's range width, from the same lengths.
-    __shared__ int s_max_len, s_sum_tiles;
-    if (threadIdx.x == 0) {
-        s_max_len = 0;
-        s_sum_tiles = 0;
-    }
-    __syncthreads();
-    for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
-        const int len = min(max(p.kv_lens[b], 0), p.Smax);
-        atomicMax(&s_max_len, len);
-        atomicAdd(&s_sum_tiles, (len + kDecBN - 1) / kDecBN);
-    }
-    __syncthreads();
-    const int W = decode_range_width(p.Hkv * s_sum_tiles, (s_max_len + kDecBN - 1) / kDecBN,
-                                     p.split_grid, p.ns);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.x * 4 + warp;  // row of [B, sq, Hq]
-    if (bh >= p.B * p.sq * p.Hq) return;
-    const int b = bh / (p.sq * p.Hq);
-    const int s_tok = (bh / p.Hq) % p.sq;
-    const int hq = bh % p.Hq;
-    const int len = min(max(p.kv_lens[b], 0), p.Smax);
-    // This row's pair (b, kv head) starts after the tiles of all earlier pairs; it has one
-    // partial per CTA range it meets.
-    int before = 0;  // tiles of one pair of each sequence before b
-    for (int bb = lane; bb < b; bb += 32) before += (min(max(p.kv_lens[bb], 0), p.Smax) + kDecBN - 1) / kDecBN;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
-    const int tb = (len + kDecBN - 1) / kDecBN;
-    const int pstart = p.Hkv * before + (hq / p.group) * tb;
-    const int n = tb > 0 ? (pstart + tb - 1) / W - pstart / W + 1 : 0;
-    const float kNegInf = -__int_as_float(0x7f800000);
-    const float kLog2e = 1.4426950408889634f;
-    const float* lrow = p.lse_part + (size_t)bh * p.ns;
-    const float* orow = p.o_part + (size_t)bh * p.ns * kDecD;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float lse = kNegInf;
-    // The partials are written by the split kernel, which may still be running when this
-    // grid starts (programmatic dependent launch): wait for its completion here.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    float m = kNegInf;
-    for (int c = lane; c < n; c += 32) m = fmaxf(m, lrow[c]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    // m = -inf: no piece holds a visible key for this row (empty cache, or a causal token
-    // that sees none): O = 0, LSE = -inf.
-    if (n > 0 && m != kNegInf) {
-        float s = 0.f;
-        for (int c = lane; c < n; c += 32) s += ex2_approx((lrow[c] - m) * kLog2e);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        // fixed summation order over the pieces; four loads in flight per lane
-        int c = 0;
-        for (; c + 4 <= n; c += 4) {
-            float4 v[4];
-            float w[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                v[u] = *reinterpret_cast<const float4*>(orow + (size_t)(c + u) * kDecD + lane * 4);
-                w[u] = ex2_approx((lrow[c + u] - m) * kLog2e);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                acc[0] = fmaf(w[u], v[u].x, acc[0]);
-                acc[1] = fmaf(w[u], v[u].y, acc[1]);
-                acc[2] = fmaf(w[u], v[u].z, acc[2]);
-                acc[3] = fmaf(w[u], v[u].w, acc[3]);
-            }
-        }
-        for (; c < n; ++c) {
-            const float w = ex2_approx((lrow[c] - m) * kLog2e);
-            const float4 v = *reinterpret_cast<const float4*>(orow + (size_t)c * kDecD + lane * 4);
-            acc[0] = fmaf(w, v.x, acc[0]);
-            acc[1] = fmaf(w, v.y, acc[1]);
-            acc[2] = fmaf(w, v.z, acc[2]);
-            acc[3] = fmaf(w, v.w, acc[3]);
-        }
-        const float inv = 1.0f / s;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i] *= inv;
-        lse = m + lg2_approx(s) * 0.69314718055994531f;
-    }
-    uint16_t* out = reinterpret_cast<uint16_t*>(p.o) + (size_t)bh * kDecD + lane * 4;
-    const uint32_t w0 = pack2<kBF16>(acc[0], acc[1]);
-    const uint32_t w1 = pack2<kBF16>(acc[2], acc[3]);
-    asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(out), "r"(w0), "r"(w1) : "memory");
-    if (p.lse && lane == 0) p.lse[((size_t)b * p.Hq + hq) * p.sq + s_tok] = lse;
-}
-
-template <int GMAX, bool kBF16>
-static fa_status launch_split(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const DecParams& p, int grid, cudaStream_t s) {
-    static int attr[64] = {0};
-    auto kern = fa_decode_split_kernel<GMAX, kBF16>;
-    if (!ensure_smem_attr((const void*)kern, kDecSmemBytes, attr)) return FA_ERR_CUDA;
-    kern<<<grid, kDecThreads, kDecSmemBytes, s>>>(tq, tk, tv, p);
-    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
-}
-
 fa_status launch_decode(const DecodeArgs& a, cudaStream_t s) {
-    if (a.D != kDecD) return FA_ERR_UNSUPPORTED;
-    if (a.B > kDecMaxB) return FA_ERR_UNSUPPORTED;
-    const int g = a.Hq / a.Hkv;
-    CUtensorMap tq, tk, tv;
-    const int g_cols = (a.Hq / a.Hkv) * a.sq;  // MMA N columns in use
-    const int q_rows = a.sq == 1 ? (a.Hq < 16 ? a.Hq : 16) : a.Hq / a.Hkv;
-    // Contiguous caches are [B, Smax, Hkv, D]; paged pools are [num_pages, page_size, Hkv, D].
-    const uint64_t rows_dim = a.block_table ? (uint64_t)a.page_size : (uint64_t)a.Smax;
-    const uint64_t outer_dim = a.block_table ? (uint64_t)a.num_pages : (uint64_t)a.B;
-    if (!encode_tmap_4d_box(&tq, a.q, a.bf16, a.D, a.Hq, a.sq, a.B, q_rows, a.sq) ||
-        !encode_tmap_4d(&tk, a.k_cache, a.bf16, a.D, a.Hkv, rows_dim, outer_dim, kDecBN) ||
-        !encode_tmap_4d(&tv, a.v_cache, a.bf16, a.D, a.Hkv, rows_dim, outer_dim, kDecBN))
-        return FA_ERR_CUDA;
-    DecParams p;
-    p.B = a.B;
-    p.Hq = a.Hq;
-    p.Hkv = a.Hkv;
-    p.group = g;
-    p.Smax = a.Smax;
-    p.ns = a.num_splits;
-    p.scale_log2 = a.scale * 1.4426950408889634f;
-    p.kv_lens = a.kv_lens;
-    p.o_part = a.o_part;
-    p.lse_part = a.lse_part;
-    p.o = a.o;
-    p.lse = a.lse;
-    p.status = a.dev_status;
-    p.q_rows = q_rows;
-    p.sq = a.sq;
-    p.causal = a.causal ? 1 : 0;
-    p.block_table = a.block_table;
-    p.page_size = a.page_size;
-    p.max_pages = a.max_pages;
-    // One CTA per SM; the kernel cuts the work into equal ranges of tiles, one per CTA.
-    const int grid = a.num_sms;
-    p.split_grid = grid;
-    fa_status st;
-    if (g_cols > 16) return FA_ERR_UNSUPPORTED;
-    if (g_cols <= 4)
-        st = a.bf16 ? launch_split<4, true>(tq, tk, tv, p, grid, s) : launch_split<4, false>(tq, tk, tv, p, grid, s);
-    else if (g_cols <= 8)
-        st = a.bf16 ? launch_split<8, true>(tq, tk, tv, p, grid, s) : launch_split<8, false>(tq, tk, tv, p, grid, s);
-    else
-        st = a.bf16 ? launch_split<16, true>(tq, tk, tv, p, grid, s) : launch_split<16, false>(tq, tk, tv, p, grid, s);
-    if (st != FA_OK) return st;
-    // The merge kernel is launched as a programmatic dependent of the split kernel: its
-    // launch overlaps the split kernel's tail, and it waits for the split results itself.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((a.B * a.sq * a.Hq + 3) / 4));
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e = a.bf16 ? cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<true>, p)
-                                 : cudaLaunchKernelEx(&cfg, fa_decode_combine_kernel<false>, p);
-    if (e != cudaSuccess) return FA_ERR_CUDA;
-    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    switch (a.D) {
+        case 64: return launch_decode_d64(a, s);
+        case 96: return launch_decode_d96(a, s);
+        case 128: return launch_decode_d128(a, s);
+        case 256: return launch_decode_d256(a, s);
+        default: return FA_ERR_UNSUPPORTED;
+    }
 }
 
 }  // namespace fa

@@ -68,6 +68,10 @@ fa_status launch_fwd_d128(const FwdArgs& a, cudaStream_t s);
 fa_status launch_fwd_d256(const FwdArgs& a, cudaStream_t s);
 
 fa_status launch_decode(const DecodeArgs& a, cudaStream_t s);
+fa_status launch_decode_d64(const DecodeArgs& a, cudaStream_t s);
+fa_status launch_decode_d96(const DecodeArgs& a, cudaStream_t s);
+fa_status launch_decode_d128(const DecodeArgs& a, cudaStream_t s);
+fa_status launch_decode_d256(const DecodeArgs& a, cudaStream_t s);
 
 // Argument checks shared by every decode entry point (pointers, alignment, sizes, dtype,
 // head dim, group size); FA_OK or the status the entry point returns.  Host only.

@@ -79,6 +79,9 @@ PREFILL_LONG = [FwdWorkload("prefill_long_s8192", 16, 8192, 8192, 32, 32, 128, c
 GQA_SWEEP = [FwdWorkload(f"gqa_d{d}", 4, 4096, 4096, 32, 8, d, True, amp=0.5, seed=1003)
              for d in (64, 96, 128, 256)]
 DECODE = DecodeWorkload("decode_splitkv", 8, 32, 8, 128, 32768, 1024, 32768, seed=1004)
+# The decode workload at the other head dims (same seed, so the same KV lengths).
+DECODE_D_SWEEP = [DecodeWorkload(f"decode_splitkv_d{d}", 8, 32, 8, d, 32768, 1024, 32768, seed=1004)
+                  for d in (64, 96, 256)]
 
 
 def fwd_inputs(w: FwdWorkload):

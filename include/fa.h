@@ -146,7 +146,8 @@ FA_API int fa_decode_default_splits(int B, int Hkv, int max_kv_len, int num_sms)
  *            output and log-sum-exp, and a second kernel merges each pair's pieces.
  *   workspace   device memory of at least fa_decode_workspace_bytes(B, Hq, D, num_splits)
  *            bytes (after the default is applied); its contents need no initialisation.
- * Sizes: B, Hq, Hkv, Smax >= 1; B <= 1024; D == 128; Hq % Hkv == 0; Hq / Hkv <= 16.
+ * Sizes: B, Hq, Hkv, Smax >= 1; B <= 1024; D in {64, 96, 128, 256}; Hq % Hkv == 0;
+ * Hq / Hkv <= 16.
  * The result does not depend on num_splits beyond fp32 rounding.  Values of kv_lens
  * outside [0, Smax] are the caller's error and are clamped on the device.
  */

@@ -86,7 +86,9 @@ def test_decode_argument_validation(lib):
     assert L.fa_decode_splitkv(*base[:3], None, *base[4:]) == 1          # null kv_lens
     bad = list(base); bad[7] = 7                                         # 7 heads over 2
     assert L.fa_decode_splitkv(*bad) == 1
-    bad = list(base); bad[9] = 96                                        # head dim 96
+    bad = list(base); bad[9] = 80                                        # head dim 80
+    assert L.fa_decode_splitkv(*bad) == 2
+    bad = list(base); bad[9] = 512                                       # head dim 512
     assert L.fa_decode_splitkv(*bad) == 2
     bad = list(base); bad[7] = 64; bad[8] = 2                            # group of 32 > 16
     assert L.fa_decode_splitkv(*bad) == 2

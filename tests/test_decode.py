@@ -75,21 +75,26 @@ def _pieces(lens, Hkv, ns, grid):
     return out
 
 
-@pytest.mark.parametrize("ns", [1, 2, 3, 7, 16])
-def test_decode_matches_oracle(fa, ns):
-    q, kc, vc, _ = inputs.make_decode(3, 8, 2, 128, 700, 1, 700, seed=50 + ns)
+HEAD_DIMS = [64, 96, 128, 256]
+
+
+@pytest.mark.parametrize("D,ns", [(d, n) for d in HEAD_DIMS for n in (1, 3, 16)]
+                         + [(128, 2), (128, 7)])
+def test_decode_matches_oracle(fa, D, ns):
+    q, kc, vc, _ = inputs.make_decode(3, 8, 2, D, 700, 1, 700, seed=50 + ns + D)
     lens = torch.tensor([700, 1, 333], dtype=torch.int32)
     o, lse = fa.fa_decode_splitkv(*_dev(q, kc, vc, lens), num_splits=ns)
     torch.cuda.synchronize()
     assert fa.fa_last_device_status() == 0
-    o_ref, lse_ref = oracle.decode(q, kc, vc, lens, scale=1 / math.sqrt(128))
+    o_ref, lse_ref = oracle.decode(q, kc, vc, lens, scale=1 / math.sqrt(D))
     _check(o, lse, o_ref, lse_ref)
 
 
-@pytest.mark.parametrize("ns", [2, 4, 64])
-def test_decode_partials_match_oracle_pieces(fa, ns):
+@pytest.mark.parametrize("D,ns", [(128, 2), (128, 4), (128, 64), (64, 5), (96, 3), (256, 4),
+                                  (256, 64)])
+def test_decode_partials_match_oracle_pieces(fa, D, ns):
     """The workspace holds, per (b, head, piece), the piece's own attention and LSE."""
-    B, Hq, Hkv, D, Smax = 3, 8, 2, 128, 3000
+    B, Hq, Hkv, Smax = 3, 8, 2, 3000
     q, kc, vc, _ = inputs.make_decode(B, Hq, Hkv, D, Smax, 1, Smax, seed=61 + ns)
     lens = torch.tensor([3000, 250, 1300], dtype=torch.int32)
     nbytes = fa.fa_decode_workspace_bytes(B, Hq, D, ns)
@@ -135,21 +140,23 @@ def test_decode_all_empty(fa):
     assert torch.all(lse == float("-inf"))
 
 
-@pytest.mark.parametrize("g", [1, 2, 3, 4, 8, 16])
-def test_decode_group_sizes(fa, g):
+@pytest.mark.parametrize("g,D", [(1, 128), (2, 128), (3, 128), (4, 128), (8, 128), (16, 128),
+                                 (16, 64), (16, 256), (3, 96)])
+def test_decode_group_sizes(fa, g, D):
     Hkv = 2
-    q, kc, vc, lens = inputs.make_decode(2, g * Hkv, Hkv, 128, 520, 1, 520, seed=70 + g)
+    q, kc, vc, lens = inputs.make_decode(2, g * Hkv, Hkv, D, 520, 1, 520, seed=70 + g)
     o, lse = fa.fa_decode_splitkv(*_dev(q, kc, vc, lens), num_splits=5)
     torch.cuda.synchronize()
-    o_ref, lse_ref = oracle.decode(q, kc, vc, lens, scale=1 / math.sqrt(128))
+    o_ref, lse_ref = oracle.decode(q, kc, vc, lens, scale=1 / math.sqrt(D))
     _check(o, lse, o_ref, lse_ref)
 
 
-def test_decode_fp16(fa):
-    q, kc, vc, lens = inputs.make_decode(3, 8, 2, 128, 640, 1, 640, seed=80, dtype="fp16")
+@pytest.mark.parametrize("D", HEAD_DIMS)
+def test_decode_fp16(fa, D):
+    q, kc, vc, lens = inputs.make_decode(3, 8, 2, D, 640, 1, 640, seed=80, dtype="fp16")
     o, lse = fa.fa_decode_splitkv(*_dev(q, kc, vc, lens), num_splits=4)
     torch.cuda.synchronize()
-    o_ref, lse_ref = oracle.decode(q, kc, vc, lens, scale=1 / math.sqrt(128))
+    o_ref, lse_ref = oracle.decode(q, kc, vc, lens, scale=1 / math.sqrt(D))
     _check(o, lse, o_ref, lse_ref)
 
 
@@ -180,11 +187,12 @@ def test_decode_one_split_equals_forward(fa):
         assert (lf[0, :, 0] - lse[b]).abs().max().item() <= LSE_TOL
 
 
-def test_decode_full_size_workload(fa):
-    """The decode workload at full size (B=8, Hq=32, Hkv=8, D=128, Smax=32768, lengths
-    U[1024, 32768]) with the default split count, launched as the benchmark launches it;
-    every output row checked against the oracle."""
-    w = inputs.DECODE
+@pytest.mark.parametrize("w", [inputs.DECODE] + inputs.DECODE_D_SWEEP, ids=lambda w: w.name)
+def test_decode_full_size_workload(fa, w):
+    """The decode workload at full size (B=8, Hq=32, Hkv=8, Smax=32768, lengths
+    U[1024, 32768]; D = 128, and the same lengths and shape at D = 64, 96 and 256) with the
+    default split count, launched as the benchmark launches it; every output row checked
+    against the oracle."""
     q, kc, vc, lens = inputs.decode_inputs(w)
     o, lse = fa.fa_decode_splitkv(*_dev(q, kc, vc, lens))
     torch.cuda.synchronize()
@@ -193,10 +201,11 @@ def test_decode_full_size_workload(fa):
     _check(o, lse, o_ref, lse_ref)
 
 
-def test_decode_output_and_workspace_guard_bands(fa):
+@pytest.mark.parametrize("D", HEAD_DIMS)
+def test_decode_output_and_workspace_guard_bands(fa, D):
     """Writes stay inside O, LSE and the workspace: sentinel pages around each are
     untouched, including with an empty sequence and a length one past a tile."""
-    B, Hq, Hkv, D, Smax, ns = 3, 8, 2, 128, 900, 4
+    B, Hq, Hkv, Smax, ns = 3, 8, 2, 900, 4
     q, kc, vc, _ = inputs.make_decode(B, Hq, Hkv, D, Smax, 1, Smax, seed=91)
     lens = torch.tensor([900, 0, 129], dtype=torch.int32)
     dev = torch.device("cuda:0")

@@ -42,19 +42,21 @@ def _make(B, Sq, Hq, Hkv, D, smax, lens, seed):
     return q, kc, vc, torch.tensor(lens, dtype=torch.int32)
 
 
-@pytest.mark.parametrize("Sq,Hq,Hkv,causal,ns", [(2, 8, 2, True, 3), (4, 8, 2, True, 5),
-                                                 (4, 8, 2, False, 2), (8, 4, 2, True, 4),
-                                                 (16, 2, 2, True, 1), (3, 6, 2, True, 7),
-                                                 (2, 16, 2, True, 2)])
-def test_multi_token_decode_matches_oracle(fa, Sq, Hq, Hkv, causal, ns):
+@pytest.mark.parametrize("Sq,Hq,Hkv,causal,ns,D", [(2, 8, 2, True, 3, 128), (4, 8, 2, True, 5, 128),
+                                                   (4, 8, 2, False, 2, 128), (8, 4, 2, True, 4, 128),
+                                                   (16, 2, 2, True, 1, 128), (3, 6, 2, True, 7, 128),
+                                                   (2, 16, 2, True, 2, 128), (4, 8, 2, True, 5, 64),
+                                                   (3, 6, 2, True, 3, 96), (4, 8, 2, True, 5, 256),
+                                                   (16, 2, 2, False, 2, 256)])
+def test_multi_token_decode_matches_oracle(fa, Sq, Hq, Hkv, causal, ns, D):
     lens = [1500, 3, 0, 777]
-    q, kc, vc, lens_t = _make(4, Sq, Hq, Hkv, 128, 1600, lens, seed=Sq * 100 + Hq)
+    q, kc, vc, lens_t = _make(4, Sq, Hq, Hkv, D, 1600, lens, seed=Sq * 100 + Hq)
     dev = torch.device("cuda:0")
     o, lse = fa.fa_decode_splitkv_multi(q.to(dev), kc.to(dev), vc.to(dev), lens_t.to(dev),
                                         causal=causal, num_splits=ns)
     torch.cuda.synchronize()
     assert fa.fa_last_device_status() == 0
-    o_ref, lse_ref = oracle.decode_multi(q, kc, vc, lens, scale=1 / math.sqrt(128), causal=causal)
+    o_ref, lse_ref = oracle.decode_multi(q, kc, vc, lens, scale=1 / math.sqrt(D), causal=causal)
     of, lf = o.float().cpu().numpy(), lse.cpu().numpy()
     fin = np.isfinite(lse_ref)
     assert np.array_equal(fin, np.isfinite(lf)), "LSE -inf pattern differs"

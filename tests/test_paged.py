@@ -53,9 +53,10 @@ def _scatter(kc, vc, page, extra_pages, seed):
     return k_pages, v_pages, table
 
 
-@pytest.mark.parametrize("page,ns", [(128, 3), (256, 5), (512, 2), (256, 16)])
-def test_paged_matches_oracle_and_contiguous(fa, page, ns):
-    B, Hq, Hkv, D, smax = 4, 16, 4, 128, 2048
+@pytest.mark.parametrize("page,ns,D", [(128, 3, 128), (256, 5, 128), (512, 2, 128), (256, 16, 128),
+                                       (128, 3, 64), (256, 5, 96), (128, 4, 256), (512, 7, 256)])
+def test_paged_matches_oracle_and_contiguous(fa, page, ns, D):
+    B, Hq, Hkv, smax = 4, 16, 4, 2048
     q, kc, vc, _ = inputs.make_decode(B, Hq, Hkv, D, smax, 1, smax, seed=500 + page)
     lens = torch.tensor([smax, 1, 0, 1234], dtype=torch.int32)
     k_pages, v_pages, table = _scatter(kc, vc, page, extra_pages=7, seed=page)
