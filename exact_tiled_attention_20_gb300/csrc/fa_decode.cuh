@@ -385,42 +385,53 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         __syncwarp();
     } else if (warp == kDecMmaWarp) {
         // ------------------------------------------------------------ MMA issuer ----
-        if (lane == 0) {
+        // The whole warp runs the issue loop: every lane waits on the barriers and the
+        // outcome is voted, and elect.sync picks the lane that issues each MMA and commit.
+        // Descriptors are built once; stepping through a tile only moves the start-address
+        // field of the low word.  (Uniform control flow keeps each small MMA cheap to issue.)
+        {
             constexpr uint32_t idesc_s = make_idesc_f16(128, 16, kBF16, false, false);
             constexpr uint32_t idesc_o = make_idesc_f16(128, 16, kBF16, true, false);
             uint32_t kv_it = 0, icount = 0, it_s = 0;
             bool ok = true;
+            auto wait = [&](uint32_t b, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait(b, parity, wc));
+            };
             const uint64_t dk0 = make_sdesc_sw128(sK, 16, 1024);
             const uint64_t dq0 = make_sdesc_sw128(sQ, 16, 1024);
             const uint64_t dv0 = make_sdesc_sw128(sV, SUB * 128, 1024);
             const uint64_t dp0 = make_sdesc_sw128(sP, 16, 1024);
+            const uint32_t k_lo = (uint32_t)dk0, k_hi = (uint32_t)(dk0 >> 32);
+            const uint32_t q_lo = (uint32_t)dq0, q_hi = (uint32_t)(dq0 >> 32);
+            const uint32_t v_lo = (uint32_t)dv0, v_hi = (uint32_t)(dv0 >> 32);
+            const uint32_t p_lo = (uint32_t)dp0, p_hi = (uint32_t)(dp0 >> 32);
             // S^T = K Q^T over the D head dims: 16 of them per MMA.
             auto issue_s = [&](uint32_t qs, uint32_t kst, uint32_t slot) {
-                const uint64_t a = dk0 + (uint64_t)((kst * DC::KVBytes) >> 4);
-                const uint64_t b = dq0 + (uint64_t)((qs * DC::QBytes) >> 4);
+                const uint32_t a = k_lo + ((kst * DC::KVBytes) >> 4);
+                const uint32_t b = q_lo + ((qs * DC::QBytes) >> 4);
                 const uint32_t d = tmem + slot * 16;
-                umma_ss_imm<false>(d, a, b, idesc_s);
+                umma_ss_elect<false>(d, a, k_hi, b, q_hi, idesc_s);
 #pragma unroll
                 for (int kk = 1; kk < D / 16; ++kk)
-                    umma_ss_imm<true>(d, a + (uint64_t)(((kk >> 2) * (SUB * 128) + (kk & 3) * 32) >> 4),
-                                      b + (uint64_t)(((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), idesc_s);
+                    umma_ss_elect<true>(d, a + (((kk >> 2) * (SUB * 128) + (kk & 3) * 32) >> 4), k_hi,
+                                        b + (((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), q_hi, idesc_s);
             };
             // O^T += V^T P^T over the SUB keys of the tile, one 128-row block of head dims
             // (two 64-dim atoms of the V tile) at a time.
             auto issue_pv = [&](uint32_t vst, uint32_t pbuf, bool acc) {
-                const uint64_t b = dp0 + (uint64_t)((pbuf * DC::PBytes) >> 4);
+                const uint32_t b = p_lo + ((pbuf * DC::PBytes) >> 4);
 #pragma unroll
                 for (int ob = 0; ob < OM; ++ob) {
-                    const uint64_t a = dv0 + (uint64_t)((vst * DC::KVBytes + ob * 2 * (SUB * 128)) >> 4);
+                    const uint32_t a = v_lo + ((vst * DC::KVBytes + ob * 2 * (SUB * 128)) >> 4);
                     const uint32_t d = tmem + 32 + ob * 16;
                     if (acc)
-                        umma_ss_imm<true>(d, a, b, idesc_o);
+                        umma_ss_elect<true>(d, a, v_hi, b, p_hi, idesc_o);
                     else
-                        umma_ss_imm<false>(d, a, b, idesc_o);
+                        umma_ss_elect<false>(d, a, v_hi, b, p_hi, idesc_o);
 #pragma unroll
                     for (int kk = 1; kk < SUB / 16; ++kk)
-                        umma_ss_imm<true>(d, a + (uint64_t)((kk * (16 * 128)) >> 4),
-                                          b + (uint64_t)(((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), idesc_o);
+                        umma_ss_elect<true>(d, a + ((kk * (16 * 128)) >> 4), v_hi,
+                                            b + (((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), p_hi, idesc_o);
                 }
             };
             int x = x0;
@@ -428,49 +439,49 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             while (ok && next_segment(T, p.B, p.Hkv, x, x_end, item)) {
                 const int n = item.ntiles * DC::NSUB;  // MMA tiles of this item
                 const uint32_t qs = icount & 1u;
-                ok = mbar_wait(bar(DC::BarQFull + qs), (icount >> 1) & 1u, wc);
+                ok = wait(bar(DC::BarQFull + qs), (icount >> 1) & 1u);
                 if (!ok) break;
                 {
                     const uint32_t st = kv_it % NS;
-                    ok = mbar_wait(bar(DC::BarKFull + st), (kv_it / NS) & 1u, wc);
+                    ok = wait(bar(DC::BarKFull + st), (kv_it / NS) & 1u);
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(qs, st, it_s & 1u);
-                    umma_commit(bar(DC::BarSFull + (it_s & 1u)));
-                    umma_commit(bar(DC::BarKEmpty + st));
-                    if (n == 1) umma_commit(bar(DC::BarQEmpty + qs));
+                    umma_commit_elect(bar(DC::BarSFull + (it_s & 1u)));
+                    umma_commit_elect(bar(DC::BarKEmpty + st));
+                    if (n == 1) umma_commit_elect(bar(DC::BarQEmpty + qs));
                 }
                 for (int j = 0; j < n && ok; ++j) {
                     const uint32_t cur = kv_it + j;
                     const uint32_t st = cur % NS;
                     if (j + 1 < n) {
                         const uint32_t nst = (cur + 1) % NS;
-                        ok = mbar_wait(bar(DC::BarKFull + nst), ((cur + 1) / NS) & 1u, wc);
+                        ok = wait(bar(DC::BarKFull + nst), ((cur + 1) / NS) & 1u);
                         if (!ok) break;
                         tc_fence_after();
                         issue_s(qs, nst, (it_s + 1) & 1u);
-                        umma_commit(bar(DC::BarSFull + ((it_s + 1) & 1u)));
-                        umma_commit(bar(DC::BarKEmpty + nst));
-                        if (j + 2 == n) umma_commit(bar(DC::BarQEmpty + qs));
+                        umma_commit_elect(bar(DC::BarSFull + ((it_s + 1) & 1u)));
+                        umma_commit_elect(bar(DC::BarKEmpty + nst));
+                        if (j + 2 == n) umma_commit_elect(bar(DC::BarQEmpty + qs));
                     }
-                    ok = mbar_wait(bar(DC::BarPFull + (it_s & 1u)), (it_s >> 1) & 1u, wc);
-                    if (ok && j == 0 && icount > 0)
-                        ok = mbar_wait(bar(DC::BarODrained), (icount - 1) & 1u, wc);
-                    if (ok) ok = mbar_wait(bar(DC::BarVFull + st), (cur / NS) & 1u, wc);
+                    ok = wait(bar(DC::BarPFull + (it_s & 1u)), (it_s >> 1) & 1u);
+                    if (ok && j == 0 && icount > 0) ok = wait(bar(DC::BarODrained), (icount - 1) & 1u);
+                    if (ok) ok = wait(bar(DC::BarVFull + st), (cur / NS) & 1u);
                     if (!ok) break;
                     tc_fence_after();
                     issue_pv(st, it_s & 1u, j > 0);
-                    umma_commit(bar(DC::BarODone + (it_s & 1u)));
-                    umma_commit(bar(DC::BarVEmpty + st));
+                    umma_commit_elect(bar(DC::BarODone + (it_s & 1u)));
+                    umma_commit_elect(bar(DC::BarVEmpty + st));
                     ++it_s;
                 }
                 kv_it += n;
                 ++icount;
             }
-            umma_commit(bar(DC::BarFinal));
+            // Every MMA issued has completed before TMEM and shared memory are released.
+            umma_commit_elect(bar(DC::BarFinal));
             mbar_wait_drain(bar(DC::BarFinal), 0);
+            __syncwarp();
         }
-        __syncwarp();
     } else {
         // --------------------------------------------------------- compute warps ----
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);

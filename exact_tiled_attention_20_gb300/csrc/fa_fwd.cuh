@@ -88,7 +88,7 @@ struct FwdConfig {
     static constexpr int kTmemCols = 512;
     static_assert(kOCol0 + NQ * D <= kTmemCols, "TMEM budget");
     static_assert(D % 32 == 0 && BN % 32 == 0, "tile shape");
-    static constexpr int kThreads = 128 * NQ + 64;
+    static constexpr int kThreads = 128 * NQ + 96;
     // O-done is signalled after every P.V when S is issued ahead of P.V (NQ == 1), and
     // only after a tile's last P.V otherwise.
     static constexpr bool kOPerIter = (NQ == 1);
@@ -98,6 +98,15 @@ struct FwdConfig {
     static constexpr bool kRingBySoftmax = (NQ > 1);
     static constexpr int kProducerWarp = 4 * NQ;
     static constexpr int kMmaWarp = 4 * NQ + 1;
+    // Fixed-length batches write O through shared memory: a softmax warpgroup stages its
+    // normalised tile there in the TMA layout and this warp stores it with a TMA bulk
+    // store, so the softmax warps do not issue row-strided global stores.  The staging
+    // buffer holds up to two 64-column atoms; wider tiles (D = 256) are staged in rounds.
+    static constexpr int kStoreWarp = 4 * NQ + 2;
+    static constexpr int kStageAtoms = DA < 2 ? DA : 2;
+    static constexpr int kStageRounds = DA / kStageAtoms;
+    static constexpr int kStageBytes = kStageAtoms * BM * 128;
+    static_assert(DA % kStageAtoms == 0, "staging rounds");
     // barrier indices
     static constexpr int kBarQFull = 0;
     static constexpr int kBarQEmpty = kBarQFull + NQ;
@@ -110,11 +119,19 @@ struct FwdConfig {
     static constexpr int kBarODone = kBarPFull + NQ;
     static constexpr int kBarODrained = kBarODone + NQ;
     static constexpr int kBarFinal = kBarODrained + NQ;
-    static constexpr int kNumBars = kBarFinal + 1;
-    static constexpr int kTileBytes = NQ * kQBytes + 2 * NS * kKVBytes;
-    static constexpr int kSmemBytes =
-        1024 /* alignment slack */ + kTileBytes + 8 * kNumBars + 16 + (int)sizeof(VarlenTable);
-    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static constexpr int kBarStaged = kBarFinal + 1;     // a warpgroup staged one round of O
+    static constexpr int kBarStageFree = kBarStaged + 1;  // the store warp has read it
+    static constexpr int kNumBars = kBarStageFree + 1;
+    // Shared memory of one instantiation: the O staging buffer for fixed-length batches,
+    // the tile table for variable-length ones.
+    template <bool kVarlen>
+    struct Layout {
+        static constexpr int kStage = kVarlen ? 0 : kStageBytes;
+        static constexpr int kTileBytes = NQ * kQBytes + 2 * NS * kKVBytes + kStage;
+        static constexpr int kSmemBytes = 1024 /* alignment slack */ + kTileBytes + 8 * kNumBars + 16 +
+                                          (kVarlen ? (int)sizeof(VarlenTable) : 0);
+        static_assert(kSmemBytes <= 232448, "shared memory budget");
+    };
 };
 
 struct TileCoord {
@@ -220,10 +237,12 @@ __device__ __forceinline__ TileCoord decode_tile(const FwdParams& p, const Varle
     return c;
 }
 
-template <class C, bool kBF16>
+template <class C, bool kBF16, bool kVarlen>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const FwdParams p) {
+    using L = typename C::template Layout<kVarlen>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t base = (raw_u32 + 1023u) & ~1023u;
@@ -232,10 +251,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     const uint32_t sQ = base;
     const uint32_t sK = sQ + C::NQ * C::kQBytes;
     const uint32_t sV = sK + C::NS * C::kKVBytes;
-    const uint32_t sBar = sV + C::NS * C::kKVBytes;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_gen + C::kTileBytes + 8 * C::kNumBars);
+    const uint32_t sStage = sV + C::NS * C::kKVBytes;  // O staging (fixed-length batches)
+    const uint32_t sBar = sStage + L::kStage;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_gen + L::kTileBytes + 8 * C::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    VarlenTable* vtab = p.cu_q ? reinterpret_cast<VarlenTable*>(tmem_slot + 4) : nullptr;
+    VarlenTable* vtab = kVarlen ? reinterpret_cast<VarlenTable*>(tmem_slot + 4) : nullptr;
     auto bar = [&](int i) -> uint32_t { return sBar + 8u * (uint32_t)i; };
 
     const int warp = threadIdx.x >> 5;
@@ -246,7 +266,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < C::kNumBars; ++i) {
             const bool by_warpgroup = (i >= C::kBarPFull && i < C::kBarPFull + C::NQ) ||
-                                      (i >= C::kBarODrained && i < C::kBarODrained + C::NQ);
+                                      (i >= C::kBarODrained && i < C::kBarODrained + C::NQ) ||
+                                      i == C::kBarStaged;
             mbar_init(bar(i), by_warpgroup ? 4u : 1u);  // one elected arrive per warp
         }
         *abort_flag = 0;
@@ -260,6 +281,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
+        if (!kVarlen) prefetch_tmap(&tm_o);
     }
     int num_tiles = p.num_tiles;
     if (vtab) {
@@ -461,6 +483,36 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             mbar_wait_drain(bar(C::kBarFinal), 0);
             __syncwarp();
         }
+    } else if (warp == C::kStoreWarp) {
+        // ---------------------------------------------------------- O store warp ----
+        // Use u of the staging buffer is round rd of Q tile q of the k-th tile with keys,
+        // u = (k NQ + q) R + rd; the warpgroups stage them in that order (each waits for the
+        // previous use to be read), and this warp stores them in the same order.
+        if (!kVarlen && lane == 0) {
+            uint32_t use = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const TileCoord c = decode_tile<C>(p, vtab, t);
+                if (c.n_kv <= 0) continue;
+                for (int q = 0; q < C::NQ && ok; ++q) {
+                    for (int rd = 0; rd < C::kStageRounds; ++rd) {
+                        ok = mbar_wait(bar(C::kBarStaged), use & 1u, wc);
+                        if (!ok) break;
+                        // a box whose first row is past the sequence holds nothing to store
+                        if (c.m0 + q * C::BM < c.sq)
+                            for (int a = 0; a < C::kStageAtoms; ++a)
+                                tma_store_4d(&tm_o, sStage + a * (C::BM * 128), (rd * C::kStageAtoms + a) * 64,
+                                             c.h, c.q_base + c.m0 + q * C::BM, c.tb);
+                        bulk_commit_group();
+                        bulk_wait_read_all();
+                        mbar_arrive(bar(C::kBarStageFree));
+                        ++use;
+                    }
+                }
+            }
+            bulk_wait_all();  // every store has landed before the kernel ends
+        }
+        __syncwarp();
     } else {
         // ------------------------------------------------------ softmax warpgroups ----
         const int q = warp >> 2;
@@ -609,23 +661,51 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             f2_unpack(l2, l0, l1);
             const float l_run = l0 + l1;
             const float inv_l = (l_run > 0.f) ? 1.0f / l_run : 0.f;
-            auto store_chunk = [&](int ch, const uint32_t (&ov)[32]) {
+            // Fixed-length batches: O goes through the staging buffer in the TMA layout
+            // (128-byte swizzle: 16-byte chunk k of row r sits at chunk k ^ (r % 8)) and the
+            // store warp writes it; rows past Sq are clipped by the tensor map.  Variable-
+            // length batches store their rows directly (a 128-row box could reach into the
+            // next sequence's rows).
+            const uint32_t u0 = (tcount - 1) * (uint32_t)(C::NQ * C::kStageRounds) + (uint32_t)(q * C::kStageRounds);
+            auto stage_wait = [&](int rd) -> bool {
+                const uint32_t u = u0 + (uint32_t)rd;
+                return u == 0 || mbar_wait(bar(C::kBarStageFree), (u - 1) & 1u, wc);
+            };
+            auto stage_done = [&]() {
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::kBarStaged));
+            };
+            // 32 columns of this row (from TMEM, fp32) -> bf16/fp16, out to global memory or
+            // into the staging buffer.  col is the first column within the row.
+            auto put_chunk = [&](int col, const uint32_t (&ov)[32]) {
                 uint32_t w[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     w[i] = pack2<kBF16>(__uint_as_float(ov[2 * i]) * inv_l,
                                         __uint_as_float(ov[2 * i + 1]) * inv_l);
-                if (row_ok) {
+                if constexpr (kVarlen) {
+                    if (row_ok) {
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        st_global_v4(orow + ch * 32 + v4 * 8, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
-                                     w[4 * v4 + 3]);
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            st_global_v4(orow + col + v4 * 8, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
+                                         w[4 * v4 + 3]);
+                    }
+                } else {
+                    const int sc = col % (C::kStageAtoms * 64);  // column within the staged round
+                    const uint32_t rowb = sStage + (uint32_t)(sc / 64) * (C::BM * 128) + (uint32_t)r * 128;
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        const uint32_t k16 = (uint32_t)((sc % 64) / 8 + v4);
+                        st_shared_v4(rowb + ((k16 ^ (uint32_t)(r & 7)) << 4), w[4 * v4], w[4 * v4 + 1],
+                                     w[4 * v4 + 2], w[4 * v4 + 3]);
+                    }
                 }
             };
             if constexpr (C::D <= 128) {
                 // All of O comes out of TMEM behind one wait and the accumulator is handed
-                // back before the normalisation and the global stores, so the next tile's
-                // first P.V does not wait for them.
+                // back before the normalisation and the stores, so the next tile's first P.V
+                // does not wait for them.
                 uint32_t ov[C::D / 32][32];
 #pragma unroll
                 for (int ch = 0; ch < C::D / 32; ++ch) tmem_ld_32x32b_x32(tO + ch * 32, ov[ch]);
@@ -635,16 +715,29 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::kBarODrained + q));
+                if (!kVarlen) {
+                    ok = stage_wait(0);
+                    if (!ok) break;
+                }
 #pragma unroll
-                for (int ch = 0; ch < C::D / 32; ++ch) store_chunk(ch, ov[ch]);
+                for (int ch = 0; ch < C::D / 32; ++ch) put_chunk(ch * 32, ov[ch]);
+                if (!kVarlen) stage_done();
             } else {
+                // Wide tiles: 32 columns at a time, staged in rounds of kStageAtoms atoms.
+                constexpr int kChunksPerRound = C::kStageAtoms * 2;
 #pragma unroll
                 for (int ch = 0; ch < C::D / 32; ++ch) {
+                    if (!kVarlen && ch % kChunksPerRound == 0) {
+                        ok = stage_wait(ch / kChunksPerRound);
+                        if (!ok) break;
+                    }
                     uint32_t ov[32];
                     tmem_ld_32x32b_x32(tO + ch * 32, ov);
                     tmem_wait_ld(ov);
-                    store_chunk(ch, ov);
+                    put_chunk(ch * 32, ov);
+                    if (!kVarlen && ch % kChunksPerRound == kChunksPerRound - 1) stage_done();
                 }
+                if (!ok) break;
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::kBarODrained + q));
@@ -699,7 +792,9 @@ template <class C>
 fa_status launch_fwd_cfg(const FwdArgs& a, cudaStream_t stream) {
     static int attr_bf16[64] = {0};
     static int attr_f16[64] = {0};
-    CUtensorMap tq, tk, tv;
+    static int attr_bf16_v[64] = {0};
+    static int attr_f16_v[64] = {0};
+    CUtensorMap tq, tk, tv, to;
     const bool varlen = a.cu_q != nullptr;
     // Fixed-length batches map [B, S, H, D] as (D, H, S, B); packed variable-length
     // batches map [total, H, D] as (D, H, total, 1).
@@ -710,6 +805,10 @@ fa_status launch_fwd_cfg(const FwdArgs& a, cudaStream_t stream) {
         !encode_tmap_4d(&tk, a.k, a.bf16, a.D, a.Hkv, k_rows, outer, C::BN) ||
         !encode_tmap_4d(&tv, a.v, a.bf16, a.D, a.Hkv, k_rows, outer, C::BN))
         return FA_ERR_CUDA;
+    // O of a fixed-length batch is written by TMA stores of 128-row boxes; a packed
+    // variable-length batch is written row by row (the map is then unused).
+    if (!varlen && !encode_tmap_4d(&to, a.o, a.bf16, a.D, a.Hq, q_rows, outer, C::BM)) return FA_ERR_CUDA;
+    if (varlen) to = tq;
     FwdParams p;
     p.B = a.B;
     p.Sq = a.Sq;
@@ -753,10 +852,12 @@ fa_status launch_fwd_cfg(const FwdArgs& a, cudaStream_t stream) {
     p.o = a.o;
     p.lse = a.lse;
     p.status = a.dev_status;
-    auto kern = a.bf16 ? fa_fwd_kernel<C, true> : fa_fwd_kernel<C, false>;
-    if (!ensure_smem_attr((const void*)kern, C::kSmemBytes, a.bf16 ? attr_bf16 : attr_f16))
-        return FA_ERR_CUDA;
-    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+    auto kern = varlen ? (a.bf16 ? fa_fwd_kernel<C, true, true> : fa_fwd_kernel<C, false, true>)
+                       : (a.bf16 ? fa_fwd_kernel<C, true, false> : fa_fwd_kernel<C, false, false>);
+    const int smem = varlen ? C::template Layout<true>::kSmemBytes : C::template Layout<false>::kSmemBytes;
+    int* flags = varlen ? (a.bf16 ? attr_bf16_v : attr_f16_v) : (a.bf16 ? attr_bf16 : attr_f16);
+    if (!ensure_smem_attr((const void*)kern, smem, flags)) return FA_ERR_CUDA;
+    kern<<<grid, C::kThreads, smem, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
