@@ -68,7 +68,13 @@ constexpr int kMaxVarlenB = 1024;
 
 // Work-tile table of a variable-length batch, built by every CTA at start.
 struct VarlenTable {
-    int prefix[kMaxVarlenB + 1];  // exclusive prefix of Hq * ceil(Sq_b / (NQ * 128))
+    // Sequences are walked longest first: order[k] is the k-th longest (by query blocks,
+    // ties by index), and prefix[k] is the exclusive prefix of Hq * ceil(Sq / (NQ * 128))
+    // (of pairs of blocks, when paired) over that order.  CTAs that run together then
+    // work on blocks of the same length and stay in step, sharing K/V in L2, and the
+    // short sequences fill in at the end.
+    int order[kMaxVarlenB];
+    int prefix[kMaxVarlenB + 1];
     int q0[kMaxVarlenB + 1];      // cu_seqlens_q
     int k0[kMaxVarlenB + 1];      // cu_seqlens_k
 };
@@ -158,16 +164,17 @@ __device__ __forceinline__ TileCoord decode_tile(const FwdParams& p, const Varle
                 return c;
             }
         }
-        int lo = 0, hi = p.B;  // largest b with prefix[b] <= u
+        int lo = 0, hi = p.B;  // largest k with prefix[k] <= u
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
             if (vt->prefix[mid] <= u) lo = mid; else hi = mid;
         }
+        const int local = u - vt->prefix[lo];
+        lo = vt->order[lo];  // the sequence
         c.b = lo;
         c.sq = vt->q0[lo + 1] - vt->q0[lo];
         c.sk = vt->k0[lo + 1] - vt->k0[lo];
         nqb = (c.sq + C::NQ * C::BM - 1) / (C::NQ * C::BM);
-        const int local = u - vt->prefix[lo];
         if (p.pair_tiles) {
             const int pairs = (nqb + 1) >> 1;
             bh_local = local / pairs;
@@ -290,12 +297,27 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             vtab->k0[i] = p.cu_k[i];
         }
         __syncthreads();
+        auto qblocks = [&](int b) -> int {
+            const int sq = max(vtab->q0[b + 1] - vtab->q0[b], 0);
+            return (sq + C::NQ * C::BM - 1) / (C::NQ * C::BM);
+        };
+        // Rank of each sequence by query blocks (descending, ties by index): B <= 1024, so
+        // at most B^2 / blockDim comparisons per thread.
+        for (int i = threadIdx.x; i < p.B; i += blockDim.x) {
+            const int ni = qblocks(i);
+            int rank = 0;
+            for (int j = 0; j < p.B; ++j) {
+                const int nj = qblocks(j);
+                rank += (nj > ni) | ((nj == ni) & (j < i));
+            }
+            vtab->order[rank] = i;
+        }
+        __syncthreads();
         if (threadIdx.x == 0) {  // B <= 1024: a serial scan is a few microseconds at most
             int run = 0;
-            for (int b = 0; b < p.B; ++b) {
-                vtab->prefix[b] = run;
-                const int sq = max(vtab->q0[b + 1] - vtab->q0[b], 0);
-                const int nqb = (sq + C::NQ * C::BM - 1) / (C::NQ * C::BM);
+            for (int k = 0; k < p.B; ++k) {
+                vtab->prefix[k] = run;
+                const int nqb = qblocks(vtab->order[k]);
                 run += p.Hq * (p.pair_tiles ? (nqb + 1) / 2 : nqb);
             }
             vtab->prefix[p.B] = run;
