@@ -104,15 +104,11 @@ struct FwdConfig {
     static constexpr bool kRingBySoftmax = (NQ > 1);
     static constexpr int kProducerWarp = 4 * NQ;
     static constexpr int kMmaWarp = 4 * NQ + 1;
-    // Fixed-length batches write O through shared memory: a softmax warpgroup stages its
-    // normalised tile there in the TMA layout and this warp stores it with a TMA bulk
-    // store, so the softmax warps do not issue row-strided global stores.  The staging
-    // buffer holds up to two 64-column atoms; wider tiles (D = 256) are staged in rounds.
+    // O is written through shared memory: a softmax warpgroup stages its normalised tile
+    // there in the TMA layout and this warp stores it with TMA bulk stores, so the softmax
+    // warps do not issue row-strided global stores.  The staging buffer holds one or two
+    // 64-column atoms (see Layout); wider tiles are staged in rounds.
     static constexpr int kStoreWarp = 4 * NQ + 2;
-    static constexpr int kStageAtoms = DA < 2 ? DA : 2;
-    static constexpr int kStageRounds = DA / kStageAtoms;
-    static constexpr int kStageBytes = kStageAtoms * BM * 128;
-    static_assert(DA % kStageAtoms == 0, "staging rounds");
     // barrier indices
     static constexpr int kBarQFull = 0;
     static constexpr int kBarQEmpty = kBarQFull + NQ;
@@ -126,13 +122,18 @@ struct FwdConfig {
     static constexpr int kBarODrained = kBarODone + NQ;
     static constexpr int kBarFinal = kBarODrained + NQ;
     static constexpr int kBarStaged = kBarFinal + 1;     // a warpgroup staged one round of O
-    static constexpr int kBarStageFree = kBarStaged + 1;  // the store warp has read it
-    static constexpr int kNumBars = kBarStageFree + 1;
-    // Shared memory of one instantiation: the O staging buffer for fixed-length batches,
-    // the tile table for variable-length ones.
+    static constexpr int kBarStageFree = kBarStaged + 1;  // per Q tile: the buffer is yours
+    static constexpr int kNumBars = kBarStageFree + NQ;
+    // Shared memory of one instantiation.  Packed variable-length batches store O row by
+    // row and hold their tile table instead of a staging buffer (a 128-row box could reach
+    // into the next sequence, and a one-atom buffer staged in rounds measured slower than
+    // the row stores).
     template <bool kVarlen>
     struct Layout {
-        static constexpr int kStage = kVarlen ? 0 : kStageBytes;
+        static constexpr int kStageAtoms = DA < 2 ? DA : 2;
+        static constexpr int kStageRounds = DA / kStageAtoms;
+        static_assert(DA % kStageAtoms == 0, "staging rounds");
+        static constexpr int kStage = kVarlen ? 0 : kStageAtoms * BM * 128;
         static constexpr int kTileBytes = NQ * kQBytes + 2 * NS * kKVBytes + kStage;
         static constexpr int kSmemBytes = 1024 /* alignment slack */ + kTileBytes + 8 * kNumBars + 16 +
                                           (kVarlen ? (int)sizeof(VarlenTable) : 0);
@@ -263,6 +264,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_gen + L::kTileBytes + 8 * C::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     VarlenTable* vtab = kVarlen ? reinterpret_cast<VarlenTable*>(tmem_slot + 4) : nullptr;
+
     auto bar = [&](int i) -> uint32_t { return sBar + 8u * (uint32_t)i; };
 
     const int warp = threadIdx.x >> 5;
@@ -288,7 +290,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
-        if (!kVarlen) prefetch_tmap(&tm_o);
+        prefetch_tmap(&tm_o);
     }
     int num_tiles = p.num_tiles;
     if (vtab) {
@@ -507,9 +509,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         }
     } else if (warp == C::kStoreWarp) {
         // ---------------------------------------------------------- O store warp ----
-        // Use u of the staging buffer is round rd of Q tile q of the k-th tile with keys,
-        // u = (k NQ + q) R + rd; the warpgroups stage them in that order (each waits for the
-        // previous use to be read), and this warp stores them in the same order.
+        // The staging buffer's uses are the rounds of the Q sub-tiles, in the order (tile
+        // with keys, sub-tile q, round).  The buffer is handed from use to use: the
+        // warpgroup of use u fills it and arrives on Staged; this warp waits for Staged,
+        // stores, and once the store has read the buffer passes it on by arriving on the
+        // StageFree barrier of use u + 1's warpgroup.  Use 0 belongs to warpgroup 0, which
+        // starts out holding the buffer.  Each StageFree barrier has one waiter and completes one phase per
+        // use of its warpgroup after that warpgroup's previous one was read, so its parity
+        // waits are exact; Staged cannot run ahead of this warp either.
         if (!kVarlen && lane == 0) {
             uint32_t use = 0;
             bool ok = true;
@@ -517,17 +524,17 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 const TileCoord c = decode_tile<C>(p, vtab, t);
                 if (c.n_kv <= 0) continue;
                 for (int q = 0; q < C::NQ && ok; ++q) {
-                    for (int rd = 0; rd < C::kStageRounds; ++rd) {
+                    for (int rd = 0; rd < L::kStageRounds; ++rd) {
+                        if (use > 0) mbar_arrive(bar(C::kBarStageFree + q));  // the buffer is q's
                         ok = mbar_wait(bar(C::kBarStaged), use & 1u, wc);
                         if (!ok) break;
                         // a box whose first row is past the sequence holds nothing to store
                         if (c.m0 + q * C::BM < c.sq)
-                            for (int a = 0; a < C::kStageAtoms; ++a)
-                                tma_store_4d(&tm_o, sStage + a * (C::BM * 128), (rd * C::kStageAtoms + a) * 64,
+                            for (int a = 0; a < L::kStageAtoms; ++a)
+                                tma_store_4d(&tm_o, sStage + a * (C::BM * 128), (rd * L::kStageAtoms + a) * 64,
                                              c.h, c.q_base + c.m0 + q * C::BM, c.tb);
                         bulk_commit_group();
                         bulk_wait_read_all();
-                        mbar_arrive(bar(C::kBarStageFree));
                         ++use;
                     }
                 }
@@ -547,6 +554,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         constexpr int kSC = C::BN / 32;        // 32-column chunks of S per block
         const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
         uint32_t it = 0, tcount = 0;
+        uint32_t nstaged = 0;  // staging-buffer uses of this warpgroup so far
         bool ok = true;
 
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
@@ -683,38 +691,33 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             f2_unpack(l2, l0, l1);
             const float l_run = l0 + l1;
             const float inv_l = (l_run > 0.f) ? 1.0f / l_run : 0.f;
-            // Fixed-length batches: O goes through the staging buffer in the TMA layout
-            // (128-byte swizzle: 16-byte chunk k of row r sits at chunk k ^ (r % 8)) and the
-            // store warp writes it; rows past Sq are clipped by the tensor map.  Variable-
-            // length batches store their rows directly (a 128-row box could reach into the
-            // next sequence's rows).
-            const uint32_t u0 = (tcount - 1) * (uint32_t)(C::NQ * C::kStageRounds) + (uint32_t)(q * C::kStageRounds);
-            auto stage_wait = [&](int rd) -> bool {
-                const uint32_t u = u0 + (uint32_t)rd;
-                return u == 0 || mbar_wait(bar(C::kBarStageFree), (u - 1) & 1u, wc);
+            // O goes through the staging buffer in the TMA layout (128-byte swizzle: 16-byte
+            // chunk k of row r sits at chunk k ^ (r % 8)) and the store warp writes it; rows
+            // past Sq are clipped by the tensor map.  Sub-tiles that are not staged (partial
+            // ones of a packed variable-length batch) store their rows directly.
+            constexpr bool use_stage = !kVarlen;
+            // The i-th use of this warpgroup waits for phase i of its StageFree barrier
+            // (phase i - 1 for warpgroup 0, which holds the buffer before use 0).
+            auto stage_wait = [&]() -> bool {
+                const int ph = (int)nstaged - (q == 0 ? 1 : 0);
+                ++nstaged;
+                return ph < 0 || mbar_wait(bar(C::kBarStageFree + q), (uint32_t)ph & 1u, wc);
             };
             auto stage_done = [&]() {
                 fence_proxy_async_shared();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::kBarStaged));
             };
-            // 32 columns of this row (from TMEM, fp32) -> bf16/fp16, out to global memory or
-            // into the staging buffer.  col is the first column within the row.
+            // 32 columns of this row (from TMEM, fp32) -> bf16/fp16, into the staging buffer
+            // or out to global memory.  col is the first column within the row.
             auto put_chunk = [&](int col, const uint32_t (&ov)[32]) {
                 uint32_t w[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     w[i] = pack2<kBF16>(__uint_as_float(ov[2 * i]) * inv_l,
                                         __uint_as_float(ov[2 * i + 1]) * inv_l);
-                if constexpr (kVarlen) {
-                    if (row_ok) {
-#pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            st_global_v4(orow + col + v4 * 8, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
-                                         w[4 * v4 + 3]);
-                    }
-                } else {
-                    const int sc = col % (C::kStageAtoms * 64);  // column within the staged round
+                if (use_stage) {
+                    const int sc = col % (L::kStageAtoms * 64);  // column within the staged round
                     const uint32_t rowb = sStage + (uint32_t)(sc / 64) * (C::BM * 128) + (uint32_t)r * 128;
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4) {
@@ -722,8 +725,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                         st_shared_v4(rowb + ((k16 ^ (uint32_t)(r & 7)) << 4), w[4 * v4], w[4 * v4 + 1],
                                      w[4 * v4 + 2], w[4 * v4 + 3]);
                     }
+                } else if (row_ok) {
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        st_global_v4(orow + col + v4 * 8, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
+                                     w[4 * v4 + 3]);
                 }
             };
+            constexpr int kChunksPerRound = L::kStageAtoms * 2;  // 32-column chunks per round
             if constexpr (C::D <= 128) {
                 // All of O comes out of TMEM behind one wait and the accumulator is handed
                 // back before the normalisation and the stores, so the next tile's first P.V
@@ -737,27 +746,31 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::kBarODrained + q));
-                if (!kVarlen) {
-                    ok = stage_wait(0);
-                    if (!ok) break;
-                }
-#pragma unroll
-                for (int ch = 0; ch < C::D / 32; ++ch) put_chunk(ch * 32, ov[ch]);
-                if (!kVarlen) stage_done();
-            } else {
-                // Wide tiles: 32 columns at a time, staged in rounds of kStageAtoms atoms.
-                constexpr int kChunksPerRound = C::kStageAtoms * 2;
 #pragma unroll
                 for (int ch = 0; ch < C::D / 32; ++ch) {
-                    if (!kVarlen && ch % kChunksPerRound == 0) {
-                        ok = stage_wait(ch / kChunksPerRound);
+                    if (use_stage && ch % kChunksPerRound == 0) {
+                        ok = stage_wait();
+                        if (!ok) break;
+                    }
+                    put_chunk(ch * 32, ov[ch]);
+                    if (use_stage && (ch % kChunksPerRound == kChunksPerRound - 1 || ch == C::D / 32 - 1))
+                        stage_done();
+                }
+                if (!ok) break;
+            } else {
+                // Wide tiles: 32 columns at a time, staged in rounds.
+#pragma unroll
+                for (int ch = 0; ch < C::D / 32; ++ch) {
+                    if (use_stage && ch % kChunksPerRound == 0) {
+                        ok = stage_wait();
                         if (!ok) break;
                     }
                     uint32_t ov[32];
                     tmem_ld_32x32b_x32(tO + ch * 32, ov);
                     tmem_wait_ld(ov);
                     put_chunk(ch * 32, ov);
-                    if (!kVarlen && ch % kChunksPerRound == kChunksPerRound - 1) stage_done();
+                    if (use_stage && (ch % kChunksPerRound == kChunksPerRound - 1 || ch == C::D / 32 - 1))
+                        stage_done();
                 }
                 if (!ok) break;
                 tc_fence_before();
@@ -827,10 +840,8 @@ fa_status launch_fwd_cfg(const FwdArgs& a, cudaStream_t stream) {
         !encode_tmap_4d(&tk, a.k, a.bf16, a.D, a.Hkv, k_rows, outer, C::BN) ||
         !encode_tmap_4d(&tv, a.v, a.bf16, a.D, a.Hkv, k_rows, outer, C::BN))
         return FA_ERR_CUDA;
-    // O of a fixed-length batch is written by TMA stores of 128-row boxes; a packed
-    // variable-length batch is written row by row (the map is then unused).
-    if (!varlen && !encode_tmap_4d(&to, a.o, a.bf16, a.D, a.Hq, q_rows, outer, C::BM)) return FA_ERR_CUDA;
-    if (varlen) to = tq;
+    // O is written by TMA stores of 128-row boxes (of packed rows for a variable-length batch).
+    if (!encode_tmap_4d(&to, a.o, a.bf16, a.D, a.Hq, q_rows, outer, C::BM)) return FA_ERR_CUDA;
     FwdParams p;
     p.B = a.B;
     p.Sq = a.Sq;
