@@ -68,7 +68,6 @@ constexpr int kDecMaxB = 1024;
 constexpr int kDecThreads = 192;
 constexpr int kDecProducerWarp = 4;
 constexpr int kDecMmaWarp = 5;
-constexpr int kDecTmemCols = 64;  // S^T slots at 0 and 16, O^T blocks at 32 and 48
 constexpr int kDecMaxBars = 48;
 
 struct DecSmemTail {
@@ -89,9 +88,14 @@ template <int D_>
 struct DecCfg {
     static constexpr int D = D_;
     static constexpr int DA = (D + 63) / 64;        // 128-byte column atoms per row
-    static constexpr int SUB = D > 128 ? 64 : 128;  // keys per MMA tile (and per ring stage)
-    static constexpr int NSUB = kDecBN / SUB;       // MMA tiles per split-plan tile
-    static constexpr int NS = D <= 64 ? 6 : 3;      // ring stages: 192 KB of K/V in flight
+    // Keys per MMA step (and per ring stage): 64 at D = 256, 256 at D = 64 (a step of 128
+    // keys there carries only 32 KB, too little to cover the step's fixed costs: its
+    // barrier waits and commits, and the compute warps' cross-warp reduction), else 128.
+    static constexpr int SUB = D > 128 ? 64 : (D <= 64 ? 256 : 128);
+    static constexpr int KM = SUB >= 128 ? SUB / 128 : 1;  // 128-key M blocks of S^T per step
+    static constexpr int BOX = SUB < 128 ? SUB : 128;     // rows of one TMA box
+    static constexpr int NBOX = SUB / BOX;                // boxes per column atom per step
+    static constexpr int NS = 3;                          // ring stages: 192 KB of K/V in flight
     static constexpr int OM = (D + 127) / 128;      // 128-row blocks of O^T
     static constexpr int KVBytes = SUB * DA * 128;
     static constexpr int QBytes = DA * 16 * 128;
@@ -118,9 +122,19 @@ struct DecCfg {
     static constexpr int SmemBytes = 1024 + TileBytes + (int)sizeof(DecSmemTail);
     static_assert(NumBars <= kDecMaxBars, "barrier slots");
     static_assert(SmemBytes <= 232448, "decode shared memory budget");
-    static_assert(32 + 16 * OM <= kDecTmemCols, "TMEM budget");
+    // TMEM: two S^T slots of KM 16-column blocks each, then the O^T blocks.
+    static constexpr int SCols = 16 * KM;
+    static constexpr int OCol0 = 2 * SCols;
+    static constexpr int TmemCols = OCol0 + 16 * OM <= 64 ? 64 : 128;
+    static_assert(OCol0 + 16 * OM <= 128, "TMEM budget");
     static_assert(D % 32 == 0 && D <= 256, "head dim");
 };
+
+// MMA steps of SUB keys that cover an item of ntiles 128-key tiles.
+template <class DC>
+__device__ __forceinline__ int dec_steps(int ntiles) {
+    return (ntiles * kDecBN + DC::SUB - 1) / DC::SUB;
+}
 
 // One segment of work: keys [k0, k1) of pair (b, hk), written to partial slot c.
 struct DecItem {
@@ -233,9 +247,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t base = (raw_u32 + 1023u) & ~1023u;
     uint8_t* base_gen = smem_raw + (base - raw_u32);
-    const uint32_t sK = base;
-    const uint32_t sV = sK + NS * DC::KVBytes;
-    const uint32_t sQ = sV + NS * DC::KVBytes;
+    // The V ring comes first: an MMA's rows past the data (the second 64-dim atom of V^T at
+    // D = 64, the 64 rows past a 64-key K tile at D = 256) then read the next stage, the K
+    // ring or the Q buffers, all inside this CTA's shared memory.
+    const uint32_t sV = base;
+    const uint32_t sK = sV + NS * DC::KVBytes;
+    const uint32_t sQ = sK + NS * DC::KVBytes;
     const uint32_t sP = sQ + 2 * DC::QBytes;
     DecSmemTail& T = *reinterpret_cast<DecSmemTail*>(base_gen + DC::TileBytes);
     auto bar = [&](int i) -> uint32_t { return smem_u32(&T.bars[i]); };
@@ -254,7 +271,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         fence_mbar_init();
     }
     if (warp == kDecMmaWarp) {
-        tmem_alloc(smem_u32(&T.tmem_slot), kDecTmemCols);
+        tmem_alloc(smem_u32(&T.tmem_slot), DC::TmemCols);
         tmem_relinquish();
     }
     if (warp == kDecProducerWarp && lane == 0) {
@@ -336,29 +353,36 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 for (int a = 0; a < DA; ++a)
                     tma_load_4d(sQ + qs * DC::QBytes + a * 2048, &tm_q, bar(DC::BarQFull + qs), a * 64,
                                 it.hk * p.group, 0, it.b);
-                // Paged caches: the page of the next MMA tile is fetched while this one waits
-                // (a page holds a whole number of 128-key tiles, so no MMA tile crosses one).
+                // Paged caches: a box's page comes from the block table (a page holds a whole
+                // number of 128-key tiles, so no box crosses one).  The last step of an item
+                // may reach past its tiles (D = 64 steps are 256 keys); such keys are masked,
+                // and the table index is clamped so the lookup stays inside the table.
                 auto page_of = [&](int r) -> int {
-                    return p.block_table[(size_t)it.b * p.max_pages + r / p.page_size];
+                    return p.block_table[(size_t)it.b * p.max_pages + min(r / p.page_size, p.max_pages - 1)];
                 };
-                const int nsub = it.ntiles * DC::NSUB;
-                int next_page = (p.block_table && nsub > 0) ? page_of(it.k0) : 0;
-                for (int j = 0; j < nsub && ok; ++j) {
+                const int nsteps = dec_steps<DC>(it.ntiles);
+                for (int j = 0; j < nsteps && ok; ++j) {
                     const uint32_t st = kv_it % NS;
                     const uint32_t ph = ((kv_it / NS) & 1u) ^ 1u;
-                    const int row = it.k0 + j * SUB;
-                    int c2 = row, c3 = it.b;  // contiguous: (key row, sequence)
-                    if (p.block_table) {      // paged: (row within page, page)
-                        c2 = row % p.page_size;
-                        c3 = next_page;
-                        if (j + 1 < nsub) next_page = page_of(row + SUB);
+                    int c2[DC::NBOX], c3[DC::NBOX];
+#pragma unroll
+                    for (int bx = 0; bx < DC::NBOX; ++bx) {
+                        const int row = it.k0 + j * SUB + bx * DC::BOX;
+                        c2[bx] = row;      // contiguous: (key row, sequence)
+                        c3[bx] = it.b;
+                        if (p.block_table) {  // paged: (row within page, page)
+                            c2[bx] = row % p.page_size;
+                            c3[bx] = page_of(row);
+                        }
                     }
                     ok = mbar_wait(bar(DC::BarKEmpty + st), ph, wc);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(DC::BarKFull + st), DC::KVBytes);
                     for (int a = 0; a < DA; ++a)
-                        tma_load_4d_hint(sK + st * DC::KVBytes + a * (SUB * 128), &tm_k,
-                                         bar(DC::BarKFull + st), a * 64, it.hk, c2, c3, kv_policy);
+#pragma unroll
+                        for (int bx = 0; bx < DC::NBOX; ++bx)
+                            tma_load_4d_hint(sK + st * DC::KVBytes + a * (SUB * 128) + bx * (DC::BOX * 128), &tm_k,
+                                             bar(DC::BarKFull + st), a * 64, it.hk, c2[bx], c3[bx], kv_policy);
                     ok = mbar_wait(bar(DC::BarVEmpty + st), ph, wc);
                     if (!ok) {
                         mbar_wait_drain(bar(DC::BarKFull + st), (kv_it / NS) & 1u);
@@ -366,8 +390,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     }
                     mbar_arrive_expect_tx(bar(DC::BarVFull + st), DC::KVBytes);
                     for (int a = 0; a < DA; ++a)
-                        tma_load_4d_hint(sV + st * DC::KVBytes + a * (SUB * 128), &tm_v,
-                                         bar(DC::BarVFull + st), a * 64, it.hk, c2, c3, kv_policy);
+#pragma unroll
+                        for (int bx = 0; bx < DC::NBOX; ++bx)
+                            tma_load_4d_hint(sV + st * DC::KVBytes + a * (SUB * 128) + bx * (DC::BOX * 128), &tm_v,
+                                             bar(DC::BarVFull + st), a * 64, it.hk, c2[bx], c3[bx], kv_policy);
                     ++kv_it;
                 }
                 ++icount;
@@ -405,16 +431,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             const uint32_t q_lo = (uint32_t)dq0, q_hi = (uint32_t)(dq0 >> 32);
             const uint32_t v_lo = (uint32_t)dv0, v_hi = (uint32_t)(dv0 >> 32);
             const uint32_t p_lo = (uint32_t)dp0, p_hi = (uint32_t)(dp0 >> 32);
-            // S^T = K Q^T over the D head dims: 16 of them per MMA.
+            // S^T = K Q^T over the D head dims (16 per MMA), one M block of 128 keys at a time.
             auto issue_s = [&](uint32_t qs, uint32_t kst, uint32_t slot) {
-                const uint32_t a = k_lo + ((kst * DC::KVBytes) >> 4);
                 const uint32_t b = q_lo + ((qs * DC::QBytes) >> 4);
-                const uint32_t d = tmem + slot * 16;
-                umma_ss_elect<false>(d, a, k_hi, b, q_hi, idesc_s);
 #pragma unroll
-                for (int kk = 1; kk < D / 16; ++kk)
-                    umma_ss_elect<true>(d, a + (((kk >> 2) * (SUB * 128) + (kk & 3) * 32) >> 4), k_hi,
-                                        b + (((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), q_hi, idesc_s);
+                for (int m = 0; m < DC::KM; ++m) {
+                    const uint32_t a = k_lo + ((kst * DC::KVBytes + m * (128 * 128)) >> 4);
+                    const uint32_t d = tmem + slot * DC::SCols + m * 16;
+                    umma_ss_elect<false>(d, a, k_hi, b, q_hi, idesc_s);
+#pragma unroll
+                    for (int kk = 1; kk < D / 16; ++kk)
+                        umma_ss_elect<true>(d, a + (((kk >> 2) * (SUB * 128) + (kk & 3) * 32) >> 4), k_hi,
+                                            b + (((kk >> 2) * 2048 + (kk & 3) * 32) >> 4), q_hi, idesc_s);
+                }
             };
             // O^T += V^T P^T over the SUB keys of the tile, one 128-row block of head dims
             // (two 64-dim atoms of the V tile) at a time.
@@ -423,7 +452,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
                 for (int ob = 0; ob < OM; ++ob) {
                     const uint32_t a = v_lo + ((vst * DC::KVBytes + ob * 2 * (SUB * 128)) >> 4);
-                    const uint32_t d = tmem + 32 + ob * 16;
+                    const uint32_t d = tmem + DC::OCol0 + ob * 16;
                     if (acc)
                         umma_ss_elect<true>(d, a, v_hi, b, p_hi, idesc_o);
                     else
@@ -437,7 +466,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             int x = x0;
             DecItem item;
             while (ok && next_segment(T, p.B, p.Hkv, x, x_end, item)) {
-                const int n = item.ntiles * DC::NSUB;  // MMA tiles of this item
+                const int n = dec_steps<DC>(item.ntiles);  // MMA steps of this item
                 const uint32_t qs = icount & 1u;
                 ok = wait(bar(DC::BarQFull + qs), (icount >> 1) & 1u);
                 if (!ok) break;
@@ -498,29 +527,38 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 m_run[h] = kNegInf;
                 l_part[h] = 0.f;
             }
-            const int n = item.ntiles * DC::NSUB;
+            const int n = dec_steps<DC>(item.ntiles);
             for (int j = 0; j < n; ++j) {
                 const uint32_t slot = it_s & 1u;
                 ok = mbar_wait(bar(DC::BarSFull + slot), (it_s >> 1) & 1u, wc);
                 if (!ok) break;
                 tc_fence_after();
-                uint32_t u[16];
-                tmem_ld_32x32b_x16(lane_base + slot * 16, u);
-                tmem_wait_ld(u);
-                // TMEM lane tid holds key k0 + j SUB + tid; lanes past SUB hold no key.
-                const int key = item.k0 + j * SUB + tid;
+                // TMEM lane tid of S^T block m holds key k0 + j SUB + 128 m + tid; lanes past
+                // SUB (64-key steps) hold no key.
+                uint32_t u[DC::KM][16];
+#pragma unroll
+                for (int m = 0; m < DC::KM; ++m) tmem_ld_32x32b_x16(lane_base + slot * DC::SCols + m * 16, u[m]);
+#pragma unroll
+                for (int m = 0; m < DC::KM; ++m) tmem_wait_ld(u[m]);
                 const int ncols = g * p.sq;
                 // Token s sees keys <= len - sq + s; column h holds token h / g, so with
-                // causal tokens this key is visible to columns h >= (key - len + sq) * g.
+                // causal tokens a key is visible to columns h >= (key - len + sq) * g.
                 const int lim0 = T.lens[item.b] - p.sq;
-                const int h_lo = p.causal ? max(key - lim0, 0) * g : 0;
-                const int h_hi = (tid < SUB && key < item.k1) ? ncols : 0;  // columns [h_lo, h_hi)
-                float sv[GMAX], mx[GMAX];
+                float sv[DC::KM][GMAX], mx[GMAX];
 #pragma unroll
-                for (int h = 0; h < GMAX; ++h) {
-                    const bool vis = h >= h_lo && h < h_hi;
-                    sv[h] = vis ? __uint_as_float(u[h]) : kNegInf;
-                    mx[h] = sv[h];
+                for (int h = 0; h < GMAX; ++h) mx[h] = kNegInf;
+#pragma unroll
+                for (int m = 0; m < DC::KM; ++m) {
+                    const int kin = m * 128 + tid;  // key within the step
+                    const int key = item.k0 + j * SUB + kin;
+                    const int h_lo = p.causal ? max(key - lim0, 0) * g : 0;
+                    const int h_hi = (kin < SUB && key < item.k1) ? ncols : 0;  // columns [h_lo, h_hi)
+#pragma unroll
+                    for (int h = 0; h < GMAX; ++h) {
+                        const bool vis = h >= h_lo && h < h_hi;
+                        sv[m][h] = vis ? __uint_as_float(u[m][h]) : kNegInf;
+                        mx[h] = fmaxf(mx[h], sv[m][h]);
+                    }
                 }
                 // per-column max over this warp's 32 keys, then over the four warps
                 const float wm = warp_reduce_cols<GMAX, true>(mx, lane);
@@ -549,11 +587,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     m_run[h] = mn;
                     msub[h] = (mn == kNegInf) ? 0.f : mn;
                 }
-                float pv[GMAX];
+                float pv[DC::KM][GMAX];
 #pragma unroll
                 for (int h = 0; h < GMAX; ++h) {
-                    pv[h] = ex2_approx(fmaf(sv[h], p.scale_log2, -msub[h]));
-                    l_part[h] = l_part[h] * alpha[h] + pv[h];
+                    float ps = 0.f;
+#pragma unroll
+                    for (int m = 0; m < DC::KM; ++m) {
+                        pv[m][h] = ex2_approx(fmaf(sv[m][h], p.scale_log2, -msub[h]));
+                        ps += pv[m][h];
+                    }
+                    l_part[h] = l_part[h] * alpha[h] + ps;
                 }
                 // This tile's P^T buffer was last read by the P.V of tile it_s - 2.
                 if (it_s >= 2) {
@@ -568,18 +611,22 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
                     for (int ob = 0; ob < OM; ++ob) {
                         uint32_t ov[16];
-                        tmem_ld_32x32b_x16(lane_base + 32 + ob * 16, ov);
+                        tmem_ld_32x32b_x16(lane_base + DC::OCol0 + ob * 16, ov);
                         tmem_wait_ld(ov);
 #pragma unroll
                         for (int h = 0; h < GMAX; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
-                        tmem_st_32x32b_x16(lane_base + 32 + ob * 16, ov);
+                        tmem_st_32x32b_x16(lane_base + DC::OCol0 + ob * 16, ov);
                     }
                     tmem_wait_st();
                 }
                 const uint32_t sPb = sP + (it_s & 1u) * DC::PBytes;
-                if (tid < SUB) {
 #pragma unroll
-                    for (int h = 0; h < GMAX; ++h) st_shared_u16(pt_addr(sPb, h, tid), to16<kBF16>(pv[h]));
+                for (int m = 0; m < DC::KM; ++m) {
+                    const int kin = m * 128 + tid;
+                    if (kin < SUB) {
+#pragma unroll
+                        for (int h = 0; h < GMAX; ++h) st_shared_u16(pt_addr(sPb, h, kin), to16<kBF16>(pv[m][h]));
+                    }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -593,7 +640,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             tc_fence_after();
             uint32_t ov[OM][16];
 #pragma unroll
-            for (int ob = 0; ob < OM; ++ob) tmem_ld_32x32b_x16(lane_base + 32 + ob * 16, ov[ob]);
+            for (int ob = 0; ob < OM; ++ob) tmem_ld_32x32b_x16(lane_base + DC::OCol0 + ob * 16, ov[ob]);
             tmem_wait_ld(ov[0]);
 #pragma unroll
             for (int ob = 1; ob < OM; ++ob) tmem_wait_ld(ov[ob]);
@@ -633,7 +680,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     __syncthreads();
     if (warp == kDecMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, kDecTmemCols);
+        tmem_dealloc(tmem, DC::TmemCols);
     }
 }
 
@@ -752,8 +799,8 @@ fa_status launch_decode_d(const DecodeArgs& a, cudaStream_t s) {
     const uint64_t rows_dim = a.block_table ? (uint64_t)a.page_size : (uint64_t)a.Smax;
     const uint64_t outer_dim = a.block_table ? (uint64_t)a.num_pages : (uint64_t)a.B;
     if (!encode_tmap_4d_box(&tq, a.q, a.bf16, a.D, a.Hq, a.sq, a.B, q_rows, a.sq) ||
-        !encode_tmap_4d(&tk, a.k_cache, a.bf16, a.D, a.Hkv, rows_dim, outer_dim, DC::SUB) ||
-        !encode_tmap_4d(&tv, a.v_cache, a.bf16, a.D, a.Hkv, rows_dim, outer_dim, DC::SUB))
+        !encode_tmap_4d(&tk, a.k_cache, a.bf16, a.D, a.Hkv, rows_dim, outer_dim, DC::BOX) ||
+        !encode_tmap_4d(&tv, a.v_cache, a.bf16, a.D, a.Hkv, rows_dim, outer_dim, DC::BOX))
         return FA_ERR_CUDA;
     DecParams p;
     p.B = a.B;
