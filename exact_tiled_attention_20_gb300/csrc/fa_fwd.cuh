@@ -90,18 +90,28 @@ struct FwdConfig {
     static constexpr int kQBytes = BM * DA * 128;
     static constexpr int kKVBytes = BN * DA * 128;
     static constexpr int kSlots = (NQ == 1) ? 2 : NQ;  // S buffers in TMEM
-    static constexpr int kOCol0 = kSlots * BN;        // first O column in TMEM
+    // S ahead of P.V with two Q tiles: where S, P and O of both tiles fit in TMEM side by
+    // side (D = 64), P gets BN / 2 columns of its own instead of overwriting S.  The
+    // softmax then hands S back as soon as it has read it into registers, and the next
+    // S = Q K^T of the same tile runs while this block's exponentials are computed; the
+    // chain S -> softmax -> P.V -> S of one tile no longer paces the loop.
+    static constexpr bool kSAhead = (NQ == 2) && (NQ * BN + NQ * (BN / 2) + NQ * D <= 512);
+    static constexpr int kPCol0 = NQ * BN;  // first P column (kSAhead)
+    static constexpr int kOCol0 = kSAhead ? NQ * BN + NQ * (BN / 2) : kSlots * BN;  // first O column
     static constexpr int kTmemCols = 512;
     static_assert(kOCol0 + NQ * D <= kTmemCols, "TMEM budget");
     static_assert(D % 32 == 0 && BN % 32 == 0, "tile shape");
     static constexpr int kThreads = 128 * NQ + 96;
-    // O-done is signalled after every P.V when S is issued ahead of P.V (NQ == 1), and
-    // only after a tile's last P.V otherwise.
-    static constexpr bool kOPerIter = (NQ == 1);
-    // With two Q tiles the K/V ring stages are released by the second softmax warpgroup:
-    // S1(j) completing implies S0(j) and every earlier P.V completed, so K_j and V_{j-1}
-    // are free.  That saves the tensor pipe two tcgen05.commit per iteration.
+    // O-done is signalled after every P.V when S is issued ahead of P.V (NQ == 1, or
+    // kSAhead), and only after a tile's last P.V otherwise.
+    static constexpr bool kOPerIter = (NQ == 1) || kSAhead;
+    // With two Q tiles the K/V ring stages are released by the second softmax warpgroup.
+    // S1(j) completing implies S0(j) and every P.V issued before S1(j) completed, so K_j
+    // is free, and so is V_{j-1} (P.V of block j - 1 precedes S(j) in the issue order), or
+    // V_{j-2} with kSAhead (S(j) is issued ahead of P.V of block j - 1).  That saves the
+    // tensor pipe two tcgen05.commit per iteration.
     static constexpr bool kRingBySoftmax = (NQ > 1);
+    static constexpr uint32_t kVReleaseLag = kSAhead ? 2u : 1u;
     static constexpr int kProducerWarp = 4 * NQ;
     static constexpr int kMmaWarp = 4 * NQ + 1;
     // O is written through shared memory: a softmax warpgroup stages its normalised tile
@@ -123,7 +133,8 @@ struct FwdConfig {
     static constexpr int kBarFinal = kBarODrained + NQ;
     static constexpr int kBarStaged = kBarFinal + 1;     // a warpgroup staged one round of O
     static constexpr int kBarStageFree = kBarStaged + 1;  // per Q tile: the buffer is yours
-    static constexpr int kNumBars = kBarStageFree + NQ;
+    static constexpr int kBarSFree = kBarStageFree + NQ;  // per Q tile: S read (kSAhead)
+    static constexpr int kNumBars = kBarSFree + NQ;
     // Shared memory of one instantiation.  Packed variable-length batches store O row by
     // row and hold their tile table instead of a staging buffer (a 128-row box could reach
     // into the next sequence, and a one-atom buffer staged in rounds measured slower than
@@ -276,6 +287,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
         for (int i = 0; i < C::kNumBars; ++i) {
             const bool by_warpgroup = (i >= C::kBarPFull && i < C::kBarPFull + C::NQ) ||
                                       (i >= C::kBarODrained && i < C::kBarODrained + C::NQ) ||
+                                      (i >= C::kBarSFree && i < C::kBarSFree + C::NQ) ||
                                       i == C::kBarStaged;
             mbar_init(bar(i), by_warpgroup ? 4u : 1u);  // one elected arrive per warp
         }
@@ -426,7 +438,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             };
             auto issue_pv = [&](int q, uint32_t vst, uint32_t slot, bool acc) {
                 const uint32_t d = tmem + C::kOCol0 + q * C::D;
-                const uint32_t a = tmem + slot * C::BN;
+                const uint32_t a = C::kSAhead ? tmem + C::kPCol0 + q * (C::BN / 2) : tmem + slot * C::BN;
                 const uint32_t b = v_lo + ((vst * C::kKVBytes) >> 4);
                 if (acc)
                     umma_ts_elect<true>(d, a, b, v_hi, idesc_o);
@@ -440,7 +452,62 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 return C::NQ == 1 ? (iter & 1u) : (uint32_t)q;
             };
 
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            // kSAhead issue order per tile: S_0(0) S_1(0), then for each block j
+            // [S_0(j+1) S_1(j+1)] P.V_0(j) P.V_1(j).  S_q(j+1) waits until softmax q has
+            // read S_q(j) (SFree); P.V_q(j) waits for P_q(j).  Every SFree phase is
+            // awaited exactly once: the S issued after block `it` is that of block it + 1,
+            // in this tile or as the first block of the next one.
+            for (int t = blockIdx.x; C::kSAhead && t < num_tiles && ok; t += gridDim.x) {
+                const TileCoord c = decode_tile<C>(p, vtab, t);
+                const int n = c.n_kv;
+                if (n <= 0) continue;
+                for (int q = 0; q < C::NQ && ok; ++q) ok = wait(bar(C::kBarQFull + q), tcount & 1u);
+                if (!ok) break;
+                {
+                    const uint32_t st = kv_it % C::NS;
+                    ok = wait(bar(C::kBarKFull + st), (kv_it / C::NS) & 1u);
+                    for (int q = 0; q < C::NQ && ok; ++q) {
+                        if (it > 0) ok = wait(bar(C::kBarSFree + q), (it - 1) & 1u);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(q, st, (uint32_t)q);
+                        umma_commit_elect(bar(C::kBarSFull + q));
+                        if (n == 1) umma_commit_elect(bar(C::kBarQEmpty + q));
+                    }
+                    if (!ok) break;
+                }
+                for (int j = 0; j < n && ok; ++j) {
+                    const uint32_t cur = kv_it + j;
+                    const uint32_t st = cur % C::NS;
+                    const uint32_t nst = (cur + 1) % C::NS;
+                    if (j + 1 < n) {
+                        ok = wait(bar(C::kBarKFull + nst), ((cur + 1) / C::NS) & 1u);
+                        for (int q = 0; q < C::NQ && ok; ++q) {
+                            ok = wait(bar(C::kBarSFree + q), it & 1u);
+                            if (!ok) break;
+                            tc_fence_after();
+                            issue_s(q, nst, (uint32_t)q);
+                            umma_commit_elect(bar(C::kBarSFull + q));
+                            if (j + 2 == n) umma_commit_elect(bar(C::kBarQEmpty + q));
+                        }
+                        if (!ok) break;
+                    }
+                    ok = wait(bar(C::kBarVFull + st), (cur / C::NS) & 1u);
+                    for (int q = 0; q < C::NQ && ok; ++q) {
+                        ok = wait(bar(C::kBarPFull + q), it & 1u);
+                        if (ok && j == 0 && tcount > 0)
+                            ok = wait(bar(C::kBarODrained + q), (tcount - 1) & 1u);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(q, st, (uint32_t)q, j > 0);
+                        umma_commit_elect(bar(C::kBarODone + q));
+                    }
+                    ++it;
+                }
+                kv_it += n;
+                ++tcount;
+            }
+            for (int t = blockIdx.x; !C::kSAhead && t < num_tiles && ok; t += gridDim.x) {
                 const TileCoord c = decode_tile<C>(p, vtab, t);
                 const int n = c.n_kv;
                 if (n <= 0) continue;
@@ -587,9 +654,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 tc_fence_after();
                 if (C::kRingBySoftmax && q == C::NQ - 1 && wq == 0 && lane == 0) {
                     mbar_arrive(bar(C::kBarKEmpty + it % C::NS));  // K of this block
-                    if (it > 0) mbar_arrive(bar(C::kBarVEmpty + (it - 1) % C::NS));  // V of the last
+                    if (it >= C::kVReleaseLag)  // V of an earlier block
+                        mbar_arrive(bar(C::kBarVEmpty + (it - C::kVReleaseLag) % C::NS));
                 }
                 const uint32_t tS = lane_base + slot * C::BN;
+                // P goes over S, or into its own columns with kSAhead.
+                const uint32_t tP = C::kSAhead ? lane_base + C::kPCol0 + q * (C::BN / 2) : tS;
                 // All chunks of S are loaded before a single wait.
                 uint32_t u[kSC][32];
 #pragma unroll
@@ -597,6 +667,11 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 tmem_wait_ld(u[0]);
 #pragma unroll
                 for (int ch = 1; ch < kSC; ++ch) reg_fence(u[ch]);
+                if (C::kSAhead) {  // S is in registers: the next S of this tile may be issued
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::kBarSFree + q));
+                }
 
                 const int n0 = (c.j0 + j) * C::BN;
                 const bool need_mask =
@@ -632,12 +707,14 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 const float m_sub = (m_run == kNegInf) ? 0.f : m_run;
                 const uint64_t nm2 = f2_pack(-m_sub, -m_sub);
 
-                // P = exp2(s * scale * log2 e - m), rounded to 16 bits and written over S,
-                // 32 columns at a time.
+                // P = exp2(s * scale * log2 e - m), rounded to 16 bits and written to TMEM
+                // (over S, or into P's own columns), 32 columns at a time.  With kSAhead the
+                // P columns and O are still read by P.V of the previous block: all of P is
+                // computed first, then that P.V is awaited, then P is stored.
                 uint64_t sum2 = f2_pack(0.f, 0.f);
+                uint32_t pk[kSC][16];
 #pragma unroll
                 for (int ch = 0; ch < kSC; ++ch) {
-                    uint32_t pk[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const uint64_t a = fma2(f2_pack(__uint_as_float(u[ch][2 * i]),
@@ -648,13 +725,22 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                         const float p0 = ex2_approx(a0);
                         const float p1 = ex2_approx(a1);
                         sum2 = add2(sum2, f2_pack(p0, p1));
-                        pk[i] = pack2<kBF16>(p0, p1);
+                        pk[ch][i] = pack2<kBF16>(p0, p1);
                     }
-                    tmem_st_32x32b_x16(tS + ch * 16, pk);
+                    if (!C::kSAhead) tmem_st_32x32b_x16(tP + ch * 16, pk[ch]);
                 }
                 l2 = fma2(l2, f2_pack(alpha, alpha), sum2);
+                if (C::kSAhead) {
+                    if (j > 0) {
+                        ok = mbar_wait(bar(C::kBarODone + q), (it - 1) & 1u, wc);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+#pragma unroll
+                    for (int ch = 0; ch < kSC; ++ch) tmem_st_32x32b_x16(tP + ch * 16, pk[ch]);
+                }
 
-                if (kOPerIter && j > 0) {
+                if (C::NQ == 1 && j > 0) {
                     // NQ == 1: the next S is issued ahead of the previous P.V, so that P.V's
                     // completion is awaited here before O may be rescaled.
                     ok = mbar_wait(bar(C::kBarODone + q), (it - 1) & 1u, wc);
@@ -662,7 +748,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     tc_fence_after();
                 }
                 // NQ == 2: S of this block was issued after the previous P.V of this tile,
-                // so its completion (awaited above) implies that P.V has completed.
+                // so its completion (awaited above) implies that P.V has completed; with
+                // kSAhead that P.V was awaited before the P stores.
                 if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll
                     for (int ch = 0; ch < C::D / 32; ++ch) {
