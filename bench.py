@@ -152,10 +152,25 @@ def tensor_roofline(achieved, peaks, src, clocks, num_sms=152):
     return r
 
 
-def kernel_source_hash() -> str:
+# Sources a kernel's traffic depends on: its own files, the shared PTX layer and the ABI
+# (which encodes the tensor maps and picks the launch shape).
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": ("fa_fwd",),
+    "fa_decode_split_kernel": ("fa_decode",),
+}
+SHARED_SOURCES = ("fa_ptx.cuh", "fa_internal.h", "fa_api.cu")
+
+
+def kernel_source_files(kernel: str):
+    csrc = os.path.join(ROOT, "exact_tiled_attention_20_gb300", "csrc")
+    prefixes = KERNEL_SOURCES.get(kernel, ("",))
+    return [n for n in sorted(os.listdir(csrc)) if n in SHARED_SOURCES or n.startswith(prefixes)]
+
+
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_tiled_attention_20_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in kernel_source_files(kernel):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -172,7 +187,7 @@ def ncu_traffic(kernel: str):
     except (OSError, ValueError):
         return None
     e = d.get(kernel)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(kernel):
         return None
     return e.get("bytes_per_launch")
 

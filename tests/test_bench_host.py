@@ -39,11 +39,21 @@ def test_ncu_traffic_only_for_the_sources_it_was_taken_on(monkeypatch):
     with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
         stored = json.load(f)
     entry = stored["fa_fwd_kernel"]
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: entry["source_hash"])
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel: entry["source_hash"])
     assert bench.ncu_traffic("fa_fwd_kernel") == entry["bytes_per_launch"]
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel: "0" * 16)
     assert bench.ncu_traffic("fa_fwd_kernel") is None
     assert bench.ncu_traffic("no_such_kernel") is None
+
+
+def test_traffic_hash_covers_each_kernel_and_the_shared_layer_only():
+    fwd = bench.kernel_source_files("fa_fwd_kernel")
+    dec = bench.kernel_source_files("fa_decode_split_kernel")
+    assert "fa_fwd.cuh" in fwd and "fa_decode.cuh" in dec
+    assert not any(n.startswith("fa_decode") for n in fwd)
+    assert not any(n.startswith("fa_fwd") for n in dec)
+    for shared in ("fa_ptx.cuh", "fa_api.cu"):
+        assert shared in fwd and shared in dec
 
 
 def test_stored_traffic_is_close_to_the_algorithmic_bytes():
