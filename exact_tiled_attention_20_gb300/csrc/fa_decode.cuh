@@ -17,7 +17,11 @@
 // pair meets more than num_splits ranges.  A pair cut by range boundaries yields one
 // segment per range it meets; each segment is computed independently and writes a
 // partial output and its log-sum-exp into the pair's next slot, which the merge kernel
-// combines.
+// combines.  Where a head's row is not a whole number of 128-byte lines (D = 96: 192
+// bytes), kv heads 2k and 2k + 1 share a line at their common edge; the plan is then laid
+// over pairs of kv heads and CTAs 2r and 2r + 1 take the same range r, one head each, so
+// the two streams reach each shared line at about the same time and it is read from DRAM
+// once (DecParams::kv_pair).
 //
 // Split kernel (persistent, one CTA per SM, walking the work items):
 //  * the producer warp streams, per item, the Q rows of the query heads sharing the KV head
@@ -48,6 +52,9 @@ struct DecParams {
     float* o_part;    // [B, Hq, ns, D]
     float* lse_part;  // [B, Hq, ns]
     int split_grid;   // CTAs of the split kernel (sets the range width)
+    // 1, or 2 when kv heads are planned in pairs: range r of the plan over (b, kv heads
+    // 2k and 2k + 1) is streamed for head 2k by CTA 2r and for head 2k + 1 by CTA 2r + 1.
+    int kv_pair;
     void* o;          // [B, Hq, D]
     float* lse;       // [B, Hq] or null
     int q_rows;  // query-head rows per Q box; rows past q_rows * sq are never read
@@ -79,7 +86,7 @@ struct DecSmemTail {
     int warp_sums[4];
     int max_len;
     int width;        // W, tiles per CTA range
-    int total_tiles;  // Hkv * prefix[B]
+    int total_tiles;  // (Hkv / kv_pair) * prefix[B]
     uint32_t tmem_slot;
     int abort_flag;
 };
@@ -151,22 +158,24 @@ __device__ __forceinline__ int decode_range_width(int total_tiles, int max_pair_
     return (int)max(w, 1LL);
 }
 
-// The next segment of this CTA's range, starting at tile x (x advances past it).
-__device__ __forceinline__ bool next_segment(const DecSmemTail& t, int B, int Hkv, int& x, int end,
-                                             DecItem& it) {
+// The next segment of range `rng`, starting at tile x (x advances past it).  The plan
+// holds Hu = Hkv / kv_pair entries per sequence; entry u stands for kv heads
+// u * kv_pair .. u * kv_pair + kv_pair - 1, and this CTA computes head u * kv_pair + sub.
+__device__ __forceinline__ bool next_segment(const DecSmemTail& t, int B, int Hu, int rng, int kv_pair,
+                                             int sub, int& x, int end, DecItem& it) {
     if (x >= end) return false;
-    int lo = 0, hi = B;  // largest b with Hkv * prefix[b] <= x; that b has tiles
+    int lo = 0, hi = B;  // largest b with Hu * prefix[b] <= x; that b has tiles
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (Hkv * t.prefix[mid] <= x) lo = mid; else hi = mid;
+        if (Hu * t.prefix[mid] <= x) lo = mid; else hi = mid;
     }
     const int tb = t.prefix[lo + 1] - t.prefix[lo];
-    const int hk = (x - Hkv * t.prefix[lo]) / tb;
-    const int pstart = Hkv * t.prefix[lo] + hk * tb;  // first tile of pair (lo, hk)
+    const int hu = (x - Hu * t.prefix[lo]) / tb;
+    const int pstart = Hu * t.prefix[lo] + hu * tb;  // first tile of entry (lo, hu)
     const int seg_end = min(end, pstart + tb);
     it.b = lo;
-    it.hk = hk;
-    it.c = (int)blockIdx.x - pstart / t.width;  // ranges met by this pair before this one
+    it.hk = hu * kv_pair + sub;
+    it.c = rng - pstart / t.width;  // ranges met by this pair before this one
     it.k0 = (x - pstart) * kDecBN;
     it.k1 = min((seg_end - pstart) * kDecBN, t.lens[lo]);
     it.ntiles = seg_end - x;
@@ -324,14 +333,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // This CTA's range of the plan, and its head within a planned pair of kv heads.
+    const int rng = (int)blockIdx.x / p.kv_pair, sub = (int)blockIdx.x % p.kv_pair;
+    const int Hu = p.Hkv / p.kv_pair;
     if (tid == 0) {
-        T.total_tiles = p.Hkv * T.prefix[p.B];
-        T.width = decode_range_width(T.total_tiles, (T.max_len + kDecBN - 1) / kDecBN, (int)gridDim.x, p.ns);
+        T.total_tiles = Hu * T.prefix[p.B];
+        T.width = decode_range_width(T.total_tiles, (T.max_len + kDecBN - 1) / kDecBN,
+                                     (int)gridDim.x / p.kv_pair, p.ns);
     }
     __syncthreads();
     const uint32_t tmem = T.tmem_slot;
-    // This CTA's range of tiles.
-    const int x0 = (int)min((long long)blockIdx.x * T.width, (long long)T.total_tiles);
+    const int x0 = (int)min((long long)rng * T.width, (long long)T.total_tiles);
     const int x_end = min(x0 + T.width, T.total_tiles);
     // The merge kernel may be scheduled now; it waits for this grid's results itself.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -345,7 +357,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             const uint64_t kv_policy = l2_policy_evict_first();
             int x = x0;
             DecItem it;
-            while (ok && next_segment(T, p.B, p.Hkv, x, x_end, it)) {
+            while (ok && next_segment(T, p.B, Hu, rng, p.kv_pair, sub, x, x_end, it)) {
                 const uint32_t qs = icount & 1u;
                 ok = mbar_wait(bar(DC::BarQEmpty + qs), ((icount >> 1) & 1u) ^ 1u, wc);
                 if (!ok) break;
@@ -465,7 +477,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             };
             int x = x0;
             DecItem item;
-            while (ok && next_segment(T, p.B, p.Hkv, x, x_end, item)) {
+            while (ok && next_segment(T, p.B, Hu, rng, p.kv_pair, sub, x, x_end, item)) {
                 const int n = dec_steps<DC>(item.ntiles);  // MMA steps of this item
                 const uint32_t qs = icount & 1u;
                 ok = wait(bar(DC::BarQFull + qs), (icount >> 1) & 1u);
@@ -520,7 +532,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         bool ok = true;
         int x = x0;
         DecItem item;
-        while (ok && next_segment(T, p.B, p.Hkv, x, x_end, item)) {
+        while (ok && next_segment(T, p.B, Hu, rng, p.kv_pair, sub, x, x_end, item)) {
             float m_run[GMAX], l_part[GMAX];
 #pragma unroll
             for (int h = 0; h < GMAX; ++h) {
@@ -702,8 +714,9 @@ __global__ void __launch_bounds__(128)
         atomicAdd(&s_sum_tiles, (len + kDecBN - 1) / kDecBN);
     }
     __syncthreads();
-    const int W = decode_range_width(p.Hkv * s_sum_tiles, (s_max_len + kDecBN - 1) / kDecBN,
-                                     p.split_grid, p.ns);
+    const int Hu = p.Hkv / p.kv_pair;
+    const int W = decode_range_width(Hu * s_sum_tiles, (s_max_len + kDecBN - 1) / kDecBN,
+                                     p.split_grid / p.kv_pair, p.ns);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x * 4 + warp;  // row of [B, sq, Hq]
     if (bh >= p.B * p.sq * p.Hq) return;
@@ -711,14 +724,14 @@ __global__ void __launch_bounds__(128)
     const int s_tok = (bh / p.Hq) % p.sq;
     const int hq = bh % p.Hq;
     const int len = min(max(p.kv_lens[b], 0), p.Smax);
-    // This row's pair (b, kv head) starts after the tiles of all earlier pairs; it has one
-    // partial per CTA range it meets.
+    // This row's pair (b, kv head) starts after the tiles of all earlier plan entries; it
+    // has one partial per range it meets.
     int before = 0;  // tiles of one pair of each sequence before b
     for (int bb = lane; bb < b; bb += 32) before += (min(max(p.kv_lens[bb], 0), p.Smax) + kDecBN - 1) / kDecBN;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
     const int tb = (len + kDecBN - 1) / kDecBN;
-    const int pstart = p.Hkv * before + (hq / p.group) * tb;
+    const int pstart = Hu * before + (hq / p.group / p.kv_pair) * tb;
     const int n = tb > 0 ? (pstart + tb - 1) / W - pstart / W + 1 : 0;
     const float kNegInf = -__int_as_float(0x7f800000);
     const float kLog2e = 1.4426950408889634f;
@@ -822,8 +835,12 @@ fa_status launch_decode_d(const DecodeArgs& a, cudaStream_t s) {
     p.block_table = a.block_table;
     p.page_size = a.page_size;
     p.max_pages = a.max_pages;
-    // One CTA per SM; the kernel cuts the work into equal ranges of tiles, one per CTA.
-    const int grid = a.num_sms;
+    // One CTA per SM; the kernel cuts the work into equal ranges of tiles, one per CTA (one
+    // per pair of CTAs when kv heads are planned in pairs: rows that are not a whole number
+    // of 128-byte lines, an even Hkv and at least two SMs).
+    const bool pair = (D * 2) % 128 != 0 && a.Hkv % 2 == 0 && a.num_sms >= 2;
+    p.kv_pair = pair ? 2 : 1;
+    const int grid = pair ? a.num_sms & ~1 : a.num_sms;
     p.split_grid = grid;
     fa_status st;
     if (g_cols <= 4)

@@ -50,22 +50,28 @@ def _check(o, lse, o_ref, lse_ref):
     return do, dl
 
 
-def _pieces(lens, Hkv, ns, grid):
+def _pieces(lens, Hkv, ns, grid, D=128):
     """Key ranges of the split kernel's partials, as the API documents them: the 128-key
     tiles of all (sequence, kv head) pairs laid end to end in (b, kv head) order and cut
-    into ranges of W tiles, one per CTA.  Returns {(b, hk): [(slot, k0, k1), ...]}."""
+    into ranges of W tiles, one per CTA.  Where a head's row is not a whole number of
+    128-byte lines (D = 96) and Hkv is even, the plan is laid over pairs of kv heads (the
+    tiles of a pair count once) on an even grid, one range per pair of CTAs, and both heads
+    of a pair get the same pieces.  Returns {(b, hk): [(slot, k0, k1), ...]}."""
+    pair = 2 if (D * 2) % 128 != 0 and Hkv % 2 == 0 and grid >= 2 else 1
+    ranges = (grid & ~1) // 2 if pair == 2 else grid
+    hu = Hkv // pair
     tiles = [(n + 127) // 128 for n in lens]
     prefix = [0]
     for t in tiles:
         prefix.append(prefix[-1] + t)
-    total = Hkv * prefix[-1]
-    w = (total + grid - 1) // grid
+    total = hu * prefix[-1]
+    w = (total + ranges - 1) // ranges
     w = max(w, (max(tiles) + ns - 2) // (ns - 1)) if ns >= 2 else max(w, total)
     w = max(w, 1)
     out = {}
     for b, tb in enumerate(tiles):
         for hk in range(Hkv):
-            start = Hkv * prefix[b] + hk * tb
+            start = hu * prefix[b] + (hk // pair) * tb
             x, pieces = start, []
             while x < start + tb:
                 end = min((x // w + 1) * w, start + tb)
@@ -106,7 +112,7 @@ def test_decode_partials_match_oracle_pieces(fa, D, ns):
     o_part = ws[: rows * D * 4].view(torch.float32).view(B, Hq, ns, D).cpu().numpy()
     l_part = ws[o_bytes: o_bytes + rows * 4].view(torch.float32).view(B, Hq, ns).cpu().numpy()
     grid = torch.cuda.get_device_properties(0).multi_processor_count
-    pieces = _pieces(lens.tolist(), Hkv, ns, grid)
+    pieces = _pieces(lens.tolist(), Hkv, ns, grid, D)
     scale = 1 / math.sqrt(D)
     g = Hq // Hkv
     checked = 0
