@@ -755,26 +755,25 @@ __global__ void __launch_bounds__(128)
         for (int c = lane; c < n; c += 32) s += ex2_approx((lrow[c] - m) * kLog2e);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        // fixed summation order over the pieces; four pieces' loads in flight per lane
-        int c = 0;
-        for (; c + 4 <= n; c += 4) {
-            float v[4][V];
-            float w[4];
+        // Fixed summation order over the pieces.  All loads of a batch of NB pieces are in
+        // flight together, so a row of up to NB pieces costs one round trip to memory after
+        // the wait (slots past n reload piece n - 1 with weight 0, an exact zero).
+        constexpr int NB = V <= 4 ? 16 : 8;
+        for (int c = 0; c < n; c += NB) {
+            float v[NB][V];
+            float w[NB];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < NB; ++u) {
+                // loads from a valid piece in every slot, so the compiler can issue them all
+                const int cu = min(c + u, n - 1);
 #pragma unroll
-                for (int i = 0; i < V; ++i) v[u][i] = orow[(size_t)(c + u) * D + i * 32];
-                w[u] = ex2_approx((lrow[c + u] - m) * kLog2e);
+                for (int i = 0; i < V; ++i) v[u][i] = orow[(size_t)cu * D + i * 32];
+                w[u] = c + u < n ? ex2_approx((lrow[cu] - m) * kLog2e) : 0.f;
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < NB; ++u)
 #pragma unroll
                 for (int i = 0; i < V; ++i) acc[i] = fmaf(w[u], v[u][i], acc[i]);
-        }
-        for (; c < n; ++c) {
-            const float w = ex2_approx((lrow[c] - m) * kLog2e);
-#pragma unroll
-            for (int i = 0; i < V; ++i) acc[i] = fmaf(w, orow[(size_t)c * D + i * 32], acc[i]);
         }
         const float inv = 1.0f / s;
 #pragma unroll
