@@ -213,7 +213,7 @@ FA_API fa_status fa_decode_splitkv_paged(const void *q, const void *k_pages, con
  *    the default split count is applied, exceeds FA_DECODE_NOALLOC_SCRATCH_BYTES are
  *    rejected with FA_ERR_WORKSPACE before anything is enqueued.
  *  - Set-up: the first call on each device (with that device current) looks up the
- *    array's device address once; make that first call before any stream capture.
+ *    array's device address once and keeps it; later calls reuse it.
  *  - Sharing: every call on a device uses the same array and leaves its contents behind.
  *    Nothing in it needs to start at zero (each call writes every partial it reads), but
  *    calls whose kernels overlap on the GPU (e.g. on two streams at once) race on it.

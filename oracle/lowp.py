@@ -1,8 +1,8 @@
 """Low-precision CPU baseline -- TEST INFRASTRUCTURE ONLY.
 
 The pages' test criterion (page "flash-attention-v100", section "Tests") compares the
-error of the fast kernel with the error of "a baseline implementation in Pytorch":
-the fast kernel's maximum error must be at most twice the baseline's.  This module is
+error of the fast kernel with that of a plain PyTorch implementation: the fast kernel's
+maximum error must be at most twice the plain one's.  This module is
 that baseline, restated plainly with PyTorch CPU ops: scores accumulated in fp32 from
 the stored 16-bit inputs, an fp32 softmax, the probabilities rounded to the input dtype
 before the second product, fp32 accumulation, and one rounding of the output to the
