@@ -256,7 +256,36 @@ __device__ __forceinline__ TileCoord decode_tile(const FwdParams& p, const Varle
     return c;
 }
 
-template <class C, bool kBF16, bool kVarlen>
+// Blocks [lo, hi] of tile c (indices into its n_kv blocks) that hold a key visible to some
+// row of Q sub-tile q; the others are fully masked for that sub-tile and are skipped (no S,
+// no softmax, no P.V for it).  With two Q tiles the tile's block range is the union of
+// both sub-tiles' ranges, so under a causal mask or a window each sub-tile can have blocks
+// of the other's only.  lo > hi: no visible key (rows past the sequence, or rows that see
+// no key).  Single-tile and S-ahead configurations always take the whole range.  Only the
+// kernel instantiated for sliding windows skips (kSkip): there a tile's first and last
+// blocks are each outside one sub-tile's window.  Elsewhere the skipping code cost more
+// than it saved, so the other instantiations keep the plain loop.
+template <class C>
+__device__ __forceinline__ void sub_tile_blocks(const FwdParams& p, const TileCoord& c, int q, int& lo, int& hi) {
+    lo = 0;
+    hi = c.n_kv - 1;
+    if (C::NQ == 1 || C::kSAhead) return;
+    const int r0 = c.m0 + q * C::BM;
+    const int r1 = min(r0 + C::BM, c.sq) - 1;  // last row of the sub-tile inside the sequence
+    const int off = c.sk - c.sq;
+    long long kmax = (long long)c.sk - 1, kmin = 0;
+    if (p.has_hi) kmax = min(kmax, (long long)r1 + off + p.hi_off);
+    if (p.has_lo) kmin = max(kmin, (long long)r0 + off - p.win_left);
+    if (r0 >= c.sq || kmax < kmin) {
+        lo = 0;
+        hi = -1;
+        return;
+    }
+    lo = max(lo, (int)(kmin / C::BN) - c.j0);
+    hi = min(hi, (int)(kmax / C::BN) - c.j0);
+}
+
+template <class C, bool kBF16, bool kVarlen, bool kSkip = false>
 __global__ void __launch_bounds__(C::kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -513,13 +542,23 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 if (n <= 0) continue;
                 for (int q = 0; q < C::NQ && ok; ++q) ok = wait(bar(C::kBarQFull + q), tcount & 1u);
                 if (!ok) break;
+                // Blocks fully masked for a sub-tile get no MMAs for it; its S-full barrier is
+                // still committed (and its P-full still awaited) so every phase stays in step.
+                int blo[C::NQ], bhi[C::NQ];
+#pragma unroll
+                for (int q = 0; q < C::NQ; ++q) {
+                    blo[q] = 0;
+                    bhi[q] = n - 1;
+                    if (kSkip) sub_tile_blocks<C>(p, c, q, blo[q], bhi[q]);
+                }
+                auto live = [&](int q, int j) -> bool { return !kSkip || (j >= blo[q] && j <= bhi[q]); };
                 {
                     const uint32_t st = kv_it % C::NS;
                     // TMA-filled operands need no tcgen05 fence: the mbarrier wait orders them.
                     ok = wait(bar(C::kBarKFull + st), (kv_it / C::NS) & 1u);
                     if (!ok) break;
                     for (int q = 0; q < C::NQ; ++q) {
-                        issue_s(q, st, slot_of(q, it));
+                        if (live(q, 0)) issue_s(q, st, slot_of(q, it));
                         umma_commit_elect(bar(C::kBarSFull + slot_of(q, it)));
                     }
                     if (!C::kRingBySoftmax) umma_commit_elect(bar(C::kBarKEmpty + st));
@@ -548,14 +587,15 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                             ok = wait(bar(C::kBarODrained + q), (tcount - 1) & 1u);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_pv(q, st, slot_of(q, it), j > 0);
+                        // the sub-tile's first live block initialises O
+                        if (live(q, j)) issue_pv(q, st, slot_of(q, it), j > (kSkip ? blo[q] : 0));
                         if (kOPerIter || j + 1 == n) umma_commit_elect(bar(C::kBarODone + q));
                         if (C::NQ > 1 && more) {
                             if (q == 0) {
                                 ok = wait(bar(C::kBarKFull + nst), ((cur + 1) / C::NS) & 1u);
                                 if (!ok) break;
                             }
-                            issue_s(q, nst, slot_of(q, it + 1));
+                            if (live(q, j + 1)) issue_s(q, nst, slot_of(q, it + 1));
                             umma_commit_elect(bar(C::kBarSFull + slot_of(q, it + 1)));
                             if (!C::kRingBySoftmax && q == C::NQ - 1)
                                 umma_commit_elect(bar(C::kBarKEmpty + nst));
@@ -645,6 +685,8 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             float m_run = kNegInf;  // running max, log2 units (raw score * scale * log2 e)
             uint64_t l2 = f2_pack(0.f, 0.f);  // running sum, two interleaved partial sums
             const int tile_row0 = c.m0 + q * C::BM;
+            int blo = 0, bhi = c.n_kv - 1;  // this sub-tile's live blocks (kSkip: others skipped)
+            if (kSkip) sub_tile_blocks<C>(p, c, q, blo, bhi);
 
             for (int j = 0; j < c.n_kv; ++j) {
                 const uint32_t slot = (C::NQ == 1) ? (it & 1u) : (uint32_t)q;
@@ -656,6 +698,12 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     mbar_arrive(bar(C::kBarKEmpty + it % C::NS));  // K of this block
                     if (it >= C::kVReleaseLag)  // V of an earlier block
                         mbar_arrive(bar(C::kBarVEmpty + (it - C::kVReleaseLag) % C::NS));
+                }
+                if (kSkip && (j < blo || j > bhi)) {  // fully masked for this sub-tile: no S
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::kBarPFull + q));
+                    ++it;
+                    continue;
                 }
                 const uint32_t tS = lane_base + slot * C::BN;
                 // P goes over S, or into its own columns with kSAhead.
@@ -750,7 +798,7 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 // NQ == 2: S of this block was issued after the previous P.V of this tile,
                 // so its completion (awaited above) implies that P.V has completed; with
                 // kSAhead that P.V was awaited before the P stores.
-                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+                if (j > (kSkip ? blo : 0) && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll
                     for (int ch = 0; ch < C::D / 32; ++ch) {
                         uint32_t ov[32];
@@ -800,9 +848,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
             auto put_chunk = [&](int col, const uint32_t (&ov)[32]) {
                 uint32_t w[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    w[i] = pack2<kBF16>(__uint_as_float(ov[2 * i]) * inv_l,
-                                        __uint_as_float(ov[2 * i + 1]) * inv_l);
+                for (int i = 0; i < 16; ++i)  // kSkip: a sub-tile that saw no key left O unwritten
+                    w[i] = pack2<kBF16>(kSkip && !(inv_l > 0.f) ? 0.f : __uint_as_float(ov[2 * i]) * inv_l,
+                                        kSkip && !(inv_l > 0.f) ? 0.f : __uint_as_float(ov[2 * i + 1]) * inv_l);
                 if (use_stage) {
                     const int sc = col % (L::kStageAtoms * 64);  // column within the staged round
                     const uint32_t rowb = sStage + (uint32_t)(sc / 64) * (C::BM * 128) + (uint32_t)r * 128;
@@ -916,6 +964,8 @@ fa_status launch_fwd_cfg(const FwdArgs& a, cudaStream_t stream) {
     static int attr_f16[64] = {0};
     static int attr_bf16_v[64] = {0};
     static int attr_f16_v[64] = {0};
+    static int attr_bf16_s[64] = {0};
+    static int attr_f16_s[64] = {0};
     CUtensorMap tq, tk, tv, to;
     const bool varlen = a.cu_q != nullptr;
     // Fixed-length batches map [B, S, H, D] as (D, H, S, B); packed variable-length
@@ -974,8 +1024,18 @@ fa_status launch_fwd_cfg(const FwdArgs& a, cudaStream_t stream) {
     p.status = a.dev_status;
     auto kern = varlen ? (a.bf16 ? fa_fwd_kernel<C, true, true> : fa_fwd_kernel<C, false, true>)
                        : (a.bf16 ? fa_fwd_kernel<C, true, false> : fa_fwd_kernel<C, false, false>);
+    // Fixed-length sliding windows take the instantiation that skips a sub-tile's blocks
+    // outside its window (two Q tiles with P over S only).
+    bool skip = false;
+    if constexpr (C::NQ == 2 && !C::kSAhead) {
+        if (!varlen && a.window_left >= 0) {
+            kern = a.bf16 ? fa_fwd_kernel<C, true, false, true> : fa_fwd_kernel<C, false, false, true>;
+            skip = true;
+        }
+    }
     const int smem = varlen ? C::template Layout<true>::kSmemBytes : C::template Layout<false>::kSmemBytes;
-    int* flags = varlen ? (a.bf16 ? attr_bf16_v : attr_f16_v) : (a.bf16 ? attr_bf16 : attr_f16);
+    int* flags = varlen ? (a.bf16 ? attr_bf16_v : attr_f16_v)
+                        : skip ? (a.bf16 ? attr_bf16_s : attr_f16_s) : (a.bf16 ? attr_bf16 : attr_f16);
     if (!ensure_smem_attr((const void*)kern, smem, flags)) return FA_ERR_CUDA;
     kern<<<grid, C::kThreads, smem, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
