@@ -57,6 +57,10 @@ CASES = [
     (1, 200, 900, 2, 2, 128, 300, 0, True),     # Sq < Sk: window near the bottom-right
     (1, 500, 120, 2, 1, 128, 30, 5, False),     # Sq > Sk: leading rows see no key
     (1, 400, 400, 2, 1, 128, 0, 0, False),      # one key per row
+    # fixed-length windows skip a Q sub-tile's blocks outside its window:
+    (2, 1030, 1030, 2, 2, 128, 127, 0, True),   # short window: most blocks dead for one sub-tile
+    (1, 1100, 1100, 2, 1, 96, 200, 0, False),   # D = 96, several tiles
+    (1, 300, 300, 2, 1, 128, 50, 0, False),     # last tile's second sub-tile lies past Sq
 ]
 
 
