@@ -146,10 +146,11 @@ def test_decode_all_empty(fa):
     assert torch.all(lse == float("-inf"))
 
 
-@pytest.mark.parametrize("g,D", [(1, 128), (2, 128), (3, 128), (4, 128), (8, 128), (16, 128),
-                                 (16, 64), (16, 256), (3, 96)])
-def test_decode_group_sizes(fa, g, D):
-    Hkv = 2
+@pytest.mark.parametrize("g,D,Hkv", [(1, 128, 2), (2, 128, 2), (3, 128, 2), (4, 128, 2), (8, 128, 2),
+                                     (16, 128, 2), (16, 64, 2), (16, 256, 2), (3, 96, 2),
+                                     (2, 96, 3), (1, 96, 1)])
+def test_decode_group_sizes(fa, g, D, Hkv):
+    """Group sizes 1..16; at D = 96 an even Hkv plans kv heads in pairs, an odd one does not."""
     q, kc, vc, lens = inputs.make_decode(2, g * Hkv, Hkv, D, 520, 1, 520, seed=70 + g)
     o, lse = fa.fa_decode_splitkv(*_dev(q, kc, vc, lens), num_splits=5)
     torch.cuda.synchronize()

@@ -77,6 +77,18 @@ def test_window_matches_oracle(fa, case):
     _check(o.cpu(), lse.cpu(), o_ref, lse_ref)
 
 
+@pytest.mark.parametrize("D", [96, 128])
+def test_window_fp16(fa, D):
+    """fp16 inputs through the fixed-length window kernel (the skipping instantiation)."""
+    q, k, v = inputs.make_qkv(1, 700, 700, 2, 1, D, seed=420 + D, dtype="fp16")
+    dev = torch.device("cuda:0")
+    o, lse = fa.fa_fwd(q.to(dev), k.to(dev), v.to(dev), causal=True, window=(200, 0))
+    torch.cuda.synchronize()
+    assert fa.fa_last_device_status() == 0
+    o_ref, lse_ref = oracle.fwd(q, k, v, scale=1 / math.sqrt(D), causal=True, window=(200, 0))
+    _check(o.cpu(), lse.cpu(), o_ref, lse_ref)
+
+
 def test_special_windows_reproduce_fa_fwd_bitwise(fa):
     q, k, v = (t.to("cuda:0") for t in inputs.make_qkv(2, 520, 520, 4, 2, 128, seed=410))
     o_full, l_full = fa.fa_fwd(q, k, v)
