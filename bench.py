@@ -167,13 +167,37 @@ def kernel_source_files(kernel: str):
     return [n for n in sorted(os.listdir(csrc)) if n in SHARED_SOURCES or n.startswith(prefixes)]
 
 
+def _code_only(text: str) -> str:
+    """C/CUDA source with comments removed and whitespace collapsed (string literals, such
+    as inline PTX, are kept), so that the hash follows the code and not its comments."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif text[i] == '"':
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_tiled_attention_20_gb300", "csrc")
     for name in kernel_source_files(kernel):
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -23,8 +23,14 @@
 //    TMEM for the whole KV loop; it is rescaled only when a row max grows by more than
 //    2^8 (the sum l uses the same stale max, so the final O / l is exact).
 //  * With NQ = 2 the two Q tiles ping-pong: the tensor pipe runs one tile's GEMMs while
-//    the other tile's softmax runs.  With NQ = 1 S is double-buffered instead.
-//  * Epilogue: O / l rounded to 16 bits and stored row by row; LSE = (m + log2 l) ln 2.
+//    the other tile's softmax runs.  With NQ = 1 S is double-buffered instead.  At D = 64,
+//    where S, P and O of both tiles fit in TMEM side by side, P has columns of its own and
+//    the next S of a tile is issued as soon as the softmax has read the current one.
+//  * Sliding windows (fixed-length batches) use an instantiation that skips, per Q tile,
+//    the blocks outside that tile's window.
+//  * Epilogue: O / l rounded to 16 bits, staged in shared memory in the TMA layout and
+//    written by a store warp with TMA stores (row stores for packed variable-length
+//    batches); LSE = (m + log2 l) ln 2.
 #pragma once
 
 #include <cuda.h>

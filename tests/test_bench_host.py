@@ -56,6 +56,15 @@ def test_traffic_hash_covers_each_kernel_and_the_shared_layer_only():
         assert shared in fwd and shared in dec
 
 
+def test_source_hash_ignores_comments_only():
+    a = 'int x = 1; // one\n/* block */ asm("mov.u32 %0, 1; // not a comment");\n'
+    b = 'int x = 1;\n asm("mov.u32 %0, 1; // not a comment");'
+    c = 'int x = 2;\n asm("mov.u32 %0, 1; // not a comment");'
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    assert "// not a comment" in bench._code_only(a)
+
+
 def test_stored_traffic_is_close_to_the_algorithmic_bytes():
     """The committed forward capture, scaled to the full launch, is within 10 % of the
     algorithmic bytes 2 (|Q| + |K| + |V| + |O|) + 4 B Hq S; the decode's within 2 %."""
