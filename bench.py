@@ -83,7 +83,7 @@ def parse_args(argv=None):
                     help="skip the per-workload measurements (the `configs` array)")
     ap.add_argument("--configs-only", action="store_true",
                     help="run only the per-workload measurements and print them as the line")
-    ap.add_argument("--config-reps", type=int, default=12)
+    ap.add_argument("--config-reps", type=int, default=20)
     ap.add_argument("--oracle-budget-s", type=float, default=1.5,
                     help="host seconds of oracle work per workload for its parity sample")
     ap.add_argument("--case", nargs=argparse.REMAINDER,
@@ -698,7 +698,7 @@ def sweep_configs(args, fa, device, peaks, peak_src, num_sms):
     cores = os.cpu_count() or 1
     flush = L2Flush(device)
     peak_h = float(peaks["hbm_gbs"])
-    reps, warm = args.config_reps, 3
+    reps, warm = args.config_reps, 5
     # oracle throughput on this host, to size each parity sample to the time budget
     w0 = inputs.PREFILL_MID[0]
     q0, k0, v0 = inputs.make_qkv(1, 256, 1024, 4, 4, 128, seed=1)
