@@ -735,12 +735,21 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                 if (need_mask) {
                     int kmax = c.sk - 1 - n0;
                     if (p.has_hi) kmax = min(kmax, row + off + p.hi_off - n0);
-                    const int kmin = p.has_lo ? row + off - p.win_left - n0 : -1;
+                    // (the window instantiation always has a lower bound, and keeps the one loop)
+                    if (kSkip || p.has_lo) {
+                        const int kmin = p.has_lo ? row + off - p.win_left - n0 : -1;
 #pragma unroll
-                    for (int ch = 0; ch < kSC; ++ch)
+                        for (int ch = 0; ch < kSC; ++ch)
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            u[ch][i] = ((ch * 32 + i > kmax) | (ch * 32 + i < kmin)) ? 0xff800000u : u[ch][i];
+                            for (int i = 0; i < 32; ++i)
+                                u[ch][i] = ((ch * 32 + i > kmax) | (ch * 32 + i < kmin)) ? 0xff800000u : u[ch][i];
+                    } else {  // no lower bound: one comparison per score
+#pragma unroll
+                        for (int ch = 0; ch < kSC; ++ch)
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                u[ch][i] = (ch * 32 + i > kmax) ? 0xff800000u : u[ch][i];
+                    }
                 }
                 // Row max over the BN scores: four independent chains of 3-input maxima.
                 auto sv = [&](int k) -> float { return __uint_as_float(u[k >> 5][k & 31]); };
