@@ -17,11 +17,12 @@
 // pair meets more than num_splits ranges.  A pair cut by range boundaries yields one
 // segment per range it meets; each segment is computed independently and writes a
 // partial output and its log-sum-exp into the pair's next slot, which the merge kernel
-// combines.  Where a head's row is not a whole number of 128-byte lines (D = 96: 192
-// bytes), kv heads 2k and 2k + 1 share a line at their common edge; the plan is then laid
-// over pairs of kv heads and CTAs 2r and 2r + 1 take the same range r, one head each, so
-// the two streams reach each shared line at about the same time and it is read from DRAM
-// once (DecParams::kv_pair).
+// combines.  The plan is laid over groups of g adjacent kv heads (g = 8, 4 or 2, the
+// largest that divides Hkv): a group's tiles count once, and CTAs g r .. g r + g - 1 take
+// the same range r, one head each (DecParams::kv_group).  The g streams then read, at
+// about the same time, head rows that sit side by side in memory at each key: whole
+// DRAM pages are used together, and where a row is not a whole number of 128-byte lines
+// (D = 96: 192 bytes) the line two heads share at their common edge is read once.
 //
 // Split kernel (persistent, one CTA per SM, walking the work items):
 //  * the producer warp streams, per item, the Q rows of the query heads sharing the KV head
@@ -52,9 +53,9 @@ struct DecParams {
     float* o_part;    // [B, Hq, ns, D]
     float* lse_part;  // [B, Hq, ns]
     int split_grid;   // CTAs of the split kernel (sets the range width)
-    // 1, or 2 when kv heads are planned in pairs: range r of the plan over (b, kv heads
-    // 2k and 2k + 1) is streamed for head 2k by CTA 2r and for head 2k + 1 by CTA 2r + 1.
-    int kv_pair;
+    // g, the kv heads planned as one entry: range r of the plan over (b, kv heads
+    // g k .. g k + g - 1) is streamed for head g k + i by CTA g r + i.
+    int kv_group;
     void* o;          // [B, Hq, D]
     float* lse;       // [B, Hq] or null
     int q_rows;  // query-head rows per Q box; rows past q_rows * sq are never read
@@ -72,6 +73,7 @@ struct DecParams {
 
 constexpr int kDecBN = 128;  // keys per tile of the split plan
 constexpr int kDecMaxB = 1024;
+constexpr int kDecMaxKvGroup = 8;  // most kv heads planned as one entry of the split plan
 constexpr int kDecThreads = 192;
 constexpr int kDecProducerWarp = 4;
 constexpr int kDecMmaWarp = 5;
@@ -86,7 +88,7 @@ struct DecSmemTail {
     int warp_sums[4];
     int max_len;
     int width;        // W, tiles per CTA range
-    int total_tiles;  // (Hkv / kv_pair) * prefix[B]
+    int total_tiles;  // (Hkv / kv_group) * prefix[B]
     uint32_t tmem_slot;
     int abort_flag;
 };
@@ -159,9 +161,9 @@ __device__ __forceinline__ int decode_range_width(int total_tiles, int max_pair_
 }
 
 // The next segment of range `rng`, starting at tile x (x advances past it).  The plan
-// holds Hu = Hkv / kv_pair entries per sequence; entry u stands for kv heads
-// u * kv_pair .. u * kv_pair + kv_pair - 1, and this CTA computes head u * kv_pair + sub.
-__device__ __forceinline__ bool next_segment(const DecSmemTail& t, int B, int Hu, int rng, int kv_pair,
+// holds Hu = Hkv / kv_group entries per sequence; entry u stands for kv heads
+// u * kv_group .. u * kv_group + kv_group - 1, and this CTA computes head u * kv_group + sub.
+__device__ __forceinline__ bool next_segment(const DecSmemTail& t, int B, int Hu, int rng, int kv_group,
                                              int sub, int& x, int end, DecItem& it) {
     if (x >= end) return false;
     int lo = 0, hi = B;  // largest b with Hu * prefix[b] <= x; that b has tiles
@@ -174,7 +176,7 @@ __device__ __forceinline__ bool next_segment(const DecSmemTail& t, int B, int Hu
     const int pstart = Hu * t.prefix[lo] + hu * tb;  // first tile of entry (lo, hu)
     const int seg_end = min(end, pstart + tb);
     it.b = lo;
-    it.hk = hu * kv_pair + sub;
+    it.hk = hu * kv_group + sub;
     it.c = rng - pstart / t.width;  // ranges met by this pair before this one
     it.k0 = (x - pstart) * kDecBN;
     it.k1 = min((seg_end - pstart) * kDecBN, t.lens[lo]);
@@ -333,13 +335,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // This CTA's range of the plan, and its head within a planned pair of kv heads.
-    const int rng = (int)blockIdx.x / p.kv_pair, sub = (int)blockIdx.x % p.kv_pair;
-    const int Hu = p.Hkv / p.kv_pair;
+    // This CTA's range of the plan, and its head within a planned group of kv heads.
+    const int rng = (int)blockIdx.x / p.kv_group, sub = (int)blockIdx.x % p.kv_group;
+    const int Hu = p.Hkv / p.kv_group;
     if (tid == 0) {
         T.total_tiles = Hu * T.prefix[p.B];
         T.width = decode_range_width(T.total_tiles, (T.max_len + kDecBN - 1) / kDecBN,
-                                     (int)gridDim.x / p.kv_pair, p.ns);
+                                     (int)gridDim.x / p.kv_group, p.ns);
     }
     __syncthreads();
     const uint32_t tmem = T.tmem_slot;
@@ -357,7 +359,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             const uint64_t kv_policy = l2_policy_evict_first();
             int x = x0;
             DecItem it;
-            while (ok && next_segment(T, p.B, Hu, rng, p.kv_pair, sub, x, x_end, it)) {
+            while (ok && next_segment(T, p.B, Hu, rng, p.kv_group, sub, x, x_end, it)) {
                 const uint32_t qs = icount & 1u;
                 ok = mbar_wait(bar(DC::BarQEmpty + qs), ((icount >> 1) & 1u) ^ 1u, wc);
                 if (!ok) break;
@@ -477,7 +479,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             };
             int x = x0;
             DecItem item;
-            while (ok && next_segment(T, p.B, Hu, rng, p.kv_pair, sub, x, x_end, item)) {
+            while (ok && next_segment(T, p.B, Hu, rng, p.kv_group, sub, x, x_end, item)) {
                 const int n = dec_steps<DC>(item.ntiles);  // MMA steps of this item
                 const uint32_t qs = icount & 1u;
                 ok = wait(bar(DC::BarQFull + qs), (icount >> 1) & 1u);
@@ -532,7 +534,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         bool ok = true;
         int x = x0;
         DecItem item;
-        while (ok && next_segment(T, p.B, Hu, rng, p.kv_pair, sub, x, x_end, item)) {
+        while (ok && next_segment(T, p.B, Hu, rng, p.kv_group, sub, x, x_end, item)) {
             float m_run[GMAX], l_part[GMAX];
 #pragma unroll
             for (int h = 0; h < GMAX; ++h) {
@@ -714,9 +716,9 @@ __global__ void __launch_bounds__(128)
         atomicAdd(&s_sum_tiles, (len + kDecBN - 1) / kDecBN);
     }
     __syncthreads();
-    const int Hu = p.Hkv / p.kv_pair;
+    const int Hu = p.Hkv / p.kv_group;
     const int W = decode_range_width(Hu * s_sum_tiles, (s_max_len + kDecBN - 1) / kDecBN,
-                                     p.split_grid / p.kv_pair, p.ns);
+                                     p.split_grid / p.kv_group, p.ns);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int bh = blockIdx.x * 4 + warp;  // row of [B, sq, Hq]
     if (bh >= p.B * p.sq * p.Hq) return;
@@ -731,7 +733,7 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
     const int tb = (len + kDecBN - 1) / kDecBN;
-    const int pstart = Hu * before + (hq / p.group / p.kv_pair) * tb;
+    const int pstart = Hu * before + (hq / p.group / p.kv_group) * tb;
     const int n = tb > 0 ? (pstart + tb - 1) / W - pstart / W + 1 : 0;
     const float kNegInf = -__int_as_float(0x7f800000);
     const float kLog2e = 1.4426950408889634f;
@@ -834,12 +836,17 @@ fa_status launch_decode_d(const DecodeArgs& a, cudaStream_t s) {
     p.block_table = a.block_table;
     p.page_size = a.page_size;
     p.max_pages = a.max_pages;
-    // One CTA per SM; the kernel cuts the work into equal ranges of tiles, one per CTA (one
-    // per pair of CTAs when kv heads are planned in pairs: rows that are not a whole number
-    // of 128-byte lines, an even Hkv and at least two SMs).
-    const bool pair = (D * 2) % 128 != 0 && a.Hkv % 2 == 0 && a.num_sms >= 2;
-    p.kv_pair = pair ? 2 : 1;
-    const int grid = pair ? a.num_sms & ~1 : a.num_sms;
+    // One CTA per SM; the kernel cuts the work into equal ranges of tiles, one per group of
+    // g CTAs, g the largest of 8, 4 and 2 that divides Hkv (and is at most the SM count),
+    // else 1.  The grid is the largest multiple of g up to the SM count.
+    int kvg = 1;
+    for (int c = kDecMaxKvGroup; c >= 2; c >>= 1)
+        if (a.Hkv % c == 0 && a.num_sms >= c) {
+            kvg = c;
+            break;
+        }
+    p.kv_group = kvg;
+    const int grid = a.num_sms - a.num_sms % kvg;
     p.split_grid = grid;
     fa_status st;
     if (g_cols <= 4)

@@ -144,10 +144,11 @@ FA_API int fa_decode_default_splits(int B, int Hkv, int max_kv_len, int num_sms)
  *            least ceil(T / (num_splits - 1)) for the longest pair's T tiles (with
  *            num_splits == 1 no pair is cut).  Each piece of a pair writes a partial
  *            output and log-sum-exp, and a second kernel merges each pair's pieces.
- *            When a head's row is not a whole number of 128-byte lines (D = 96) and Hkv
- *            is even, kv heads 2k and 2k + 1 are laid out as one entry (whose tiles count
- *            once) and the ranges go one per two SMs (an even count), one SM per head, so
- *            that both heads get the same pieces and read their shared lines together.
+ *            The kv heads are laid out in groups of g adjacent heads, g the largest of
+ *            8, 4 and 2 that divides Hkv (else 1): a group is one entry, whose tiles count
+ *            once, and the ranges go one per g SMs (the SM count rounded down to a
+ *            multiple of g), one SM per head, so that the heads of a group get the same
+ *            pieces and read the rows that sit side by side in the cache together.
  *   workspace   device memory of at least fa_decode_workspace_bytes(B, Hq, D, num_splits)
  *            bytes (after the default is applied); its contents need no initialisation.
  * Sizes: B, Hq, Hkv, Smax >= 1; B <= 1024; D in {64, 96, 128, 256}; Hq % Hkv == 0;

@@ -13,6 +13,7 @@ import pytest
 import torch
 
 import oracle
+from decode_plan import pieces as _pieces
 from exact_tiled_attention_20_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -50,37 +51,6 @@ def _check(o, lse, o_ref, lse_ref):
     return do, dl
 
 
-def _pieces(lens, Hkv, ns, grid, D=128):
-    """Key ranges of the split kernel's partials, as the API documents them: the 128-key
-    tiles of all (sequence, kv head) pairs laid end to end in (b, kv head) order and cut
-    into ranges of W tiles, one per CTA.  Where a head's row is not a whole number of
-    128-byte lines (D = 96) and Hkv is even, the plan is laid over pairs of kv heads (the
-    tiles of a pair count once) on an even grid, one range per pair of CTAs, and both heads
-    of a pair get the same pieces.  Returns {(b, hk): [(slot, k0, k1), ...]}."""
-    pair = 2 if (D * 2) % 128 != 0 and Hkv % 2 == 0 and grid >= 2 else 1
-    ranges = (grid & ~1) // 2 if pair == 2 else grid
-    hu = Hkv // pair
-    tiles = [(n + 127) // 128 for n in lens]
-    prefix = [0]
-    for t in tiles:
-        prefix.append(prefix[-1] + t)
-    total = hu * prefix[-1]
-    w = (total + ranges - 1) // ranges
-    w = max(w, (max(tiles) + ns - 2) // (ns - 1)) if ns >= 2 else max(w, total)
-    w = max(w, 1)
-    out = {}
-    for b, tb in enumerate(tiles):
-        for hk in range(Hkv):
-            start = hu * prefix[b] + (hk // pair) * tb
-            x, pieces = start, []
-            while x < start + tb:
-                end = min((x // w + 1) * w, start + tb)
-                pieces.append((x // w - start // w, (x - start) * 128, min((end - start) * 128, lens[b])))
-                x = end
-            out[(b, hk)] = pieces
-    return out
-
-
 HEAD_DIMS = [64, 96, 128, 256]
 
 
@@ -96,11 +66,14 @@ def test_decode_matches_oracle(fa, D, ns):
     _check(o, lse, o_ref, lse_ref)
 
 
-@pytest.mark.parametrize("D,ns", [(128, 2), (128, 4), (128, 64), (64, 5), (96, 3), (256, 4),
-                                  (256, 64)])
-def test_decode_partials_match_oracle_pieces(fa, D, ns):
-    """The workspace holds, per (b, head, piece), the piece's own attention and LSE."""
-    B, Hq, Hkv, Smax = 3, 8, 2, 3000
+@pytest.mark.parametrize("D,ns,Hkv", [(128, 2, 2), (128, 4, 2), (128, 64, 2), (64, 5, 2), (96, 3, 2),
+                                      (256, 4, 2), (256, 64, 2), (64, 5, 8), (96, 3, 4),
+                                      (128, 7, 16), (128, 4, 3), (96, 3, 6)])
+def test_decode_partials_match_oracle_pieces(fa, D, ns, Hkv):
+    """The workspace holds, per (b, head, piece), the piece's own attention and LSE; kv heads
+    in groups of 2, 4 and 8 (Hkv = 16: two groups per sequence), and none (Hkv = 3)."""
+    B, Smax = 3, 3000
+    Hq = 8 if 8 % Hkv == 0 else 2 * Hkv
     q, kc, vc, _ = inputs.make_decode(B, Hq, Hkv, D, Smax, 1, Smax, seed=61 + ns)
     lens = torch.tensor([3000, 250, 1300], dtype=torch.int32)
     nbytes = fa.fa_decode_workspace_bytes(B, Hq, D, ns)
@@ -112,7 +85,7 @@ def test_decode_partials_match_oracle_pieces(fa, D, ns):
     o_part = ws[: rows * D * 4].view(torch.float32).view(B, Hq, ns, D).cpu().numpy()
     l_part = ws[o_bytes: o_bytes + rows * 4].view(torch.float32).view(B, Hq, ns).cpu().numpy()
     grid = torch.cuda.get_device_properties(0).multi_processor_count
-    pieces = _pieces(lens.tolist(), Hkv, ns, grid, D)
+    pieces = _pieces(lens.tolist(), Hkv, ns, grid)
     scale = 1 / math.sqrt(D)
     g = Hq // Hkv
     checked = 0
@@ -148,9 +121,11 @@ def test_decode_all_empty(fa):
 
 @pytest.mark.parametrize("g,D,Hkv", [(1, 128, 2), (2, 128, 2), (3, 128, 2), (4, 128, 2), (8, 128, 2),
                                      (16, 128, 2), (16, 64, 2), (16, 256, 2), (3, 96, 2),
-                                     (2, 96, 3), (1, 96, 1)])
+                                     (2, 96, 3), (1, 96, 1), (2, 64, 8), (4, 96, 4), (1, 128, 16),
+                                     (2, 96, 6), (4, 256, 8)])
 def test_decode_group_sizes(fa, g, D, Hkv):
-    """Group sizes 1..16; at D = 96 an even Hkv plans kv heads in pairs, an odd one does not."""
+    """GQA group sizes 1..16, with kv heads planned in groups of 2, 4 and 8 where Hkv
+    allows and one by one where it is odd."""
     q, kc, vc, lens = inputs.make_decode(2, g * Hkv, Hkv, D, 520, 1, 520, seed=70 + g)
     o, lse = fa.fa_decode_splitkv(*_dev(q, kc, vc, lens), num_splits=5)
     torch.cuda.synchronize()

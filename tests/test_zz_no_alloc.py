@@ -56,8 +56,8 @@ def test_noalloc_decode_matches_workspace_decode_twice(lib):
     dev = torch.device("cuda:0")
     cases = [(inputs.make_decode(4, 32, 8, 128, 4096, 100, 4096, seed=91), 0),
              (inputs.make_decode(3, 16, 2, 128, 2500, 1, 2500, seed=92), 7),
-             (inputs.make_decode(3, 16, 4, 96, 2000, 1, 2000, seed=94), 5),   # kv heads in pairs
-             (inputs.make_decode(2, 8, 2, 64, 3000, 1, 3000, seed=95), 0)]    # 256-key steps
+             (inputs.make_decode(3, 16, 4, 96, 2000, 1, 2000, seed=94), 5),   # kv heads in fours
+             (inputs.make_decode(2, 8, 2, 64, 3000, 1, 3000, seed=95), 0)]    # 256-key steps, pairs
     for (qh, kh, vh, lh), ns in cases:
         o_def, lse_def = oracle.decode(qh, kh, vh, lh, scale=1.0 / math.sqrt(qh.shape[-1]))
         q, kc, vc, lens = (t.to(dev) for t in (qh, kh, vh, lh))
