@@ -66,7 +66,8 @@ CASES = """\
   --case fwd_window B S Hq Hkv D left right [iters]
   --case fwd_varlen_workload [iters]          16 causal sequences U[256, 8192], Hq=Hkv=32, D=128
   --case decode B Hq Hkv D Smax [iters]       lengths U[Smax/32, Smax]
-  --case decode_workload [iters]              the decode workload, default split count
+  --case decode_workload [iters] [D]          the decode workload (its lengths at head dim D,
+                                              default 128), default split count
   --case decode_paged_workload [iters]        the same in 256-key pages, random page order
 """
 
@@ -1031,8 +1032,11 @@ def run_case(argv):
         o = torch.empty_like(q)
         call = lambda: fa.fa_decode_splitkv(q, kc, vc, lens, num_splits=ns, workspace=ws, out=o)  # noqa: E731
     elif kind in ("decode_workload", "decode_paged_workload"):
-        w = inputs.DECODE
         iters = int(rest[0]) if rest else 3
+        d = int(rest[1]) if kind == "decode_workload" and len(rest) > 1 else inputs.DECODE.D
+        w = next((x for x in [inputs.DECODE] + inputs.DECODE_D_SWEEP if x.D == d), None)
+        if w is None:
+            raise SystemExit(f"no decode workload at head dim {d}")
         qh, kh, vh, lh = inputs.decode_inputs(w)
         ns = fa.fa_decode_default_splits(w.B, w.Hkv, w.Smax)
         ws = torch.empty(fa.fa_decode_workspace_bytes(w.B, w.Hq, w.D, ns), dtype=torch.uint8, device=dev)
