@@ -746,41 +746,68 @@ __global__ void __launch_bounds__(128)
     // The partials are written by the split kernel, which may still be running when this
     // grid starts (programmatic dependent launch): wait for its completion here.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    float m = kNegInf;
-    for (int c = lane; c < n; c += 32) m = fmaxf(m, lrow[c]);
+    // Up to NB pieces (all of them at the decode workload's sizes): every piece's LSE and
+    // partial output are loaded together, one round trip to memory after the wait, and
+    // each lane combines them in piece order.  More pieces: the maximum first, then
+    // batches of NB.  Slots past n reload piece n - 1 with weight 0, an exact zero.
+    constexpr int NB = V <= 4 ? 16 : 8;
+    if (n > 0 && n <= NB) {
+        float l[NB], v[NB][V];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    // m = -inf: no piece holds a visible key for this row (empty cache, or a causal token
-    // that sees none): O = 0, LSE = -inf.
-    if (n > 0 && m != kNegInf) {
-        float s = 0.f;
-        for (int c = lane; c < n; c += 32) s += ex2_approx((lrow[c] - m) * kLog2e);
+        for (int u = 0; u < NB; ++u) {
+            const int cu = min(u, n - 1);
+            l[u] = lrow[cu];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        // Fixed summation order over the pieces.  All loads of a batch of NB pieces are in
-        // flight together, so a row of up to NB pieces costs one round trip to memory after
-        // the wait (slots past n reload piece n - 1 with weight 0, an exact zero).
-        constexpr int NB = V <= 4 ? 16 : 8;
-        for (int c = 0; c < n; c += NB) {
-            float v[NB][V];
-            float w[NB];
+            for (int i = 0; i < V; ++i) v[u][i] = orow[(size_t)cu * D + i * 32];
+        }
+        float m = kNegInf;
+#pragma unroll
+        for (int u = 0; u < NB; ++u) m = fmaxf(m, l[u]);
+        // m = -inf: no piece holds a visible key for this row (a causal token that sees
+        // none): O = 0, LSE = -inf.
+        if (m != kNegInf) {
+            float s = 0.f;
 #pragma unroll
             for (int u = 0; u < NB; ++u) {
-                // loads from a valid piece in every slot, so the compiler can issue them all
-                const int cu = min(c + u, n - 1);
+                const float w = u < n ? ex2_approx((l[u] - m) * kLog2e) : 0.f;
+                s += w;
 #pragma unroll
-                for (int i = 0; i < V; ++i) v[u][i] = orow[(size_t)cu * D + i * 32];
-                w[u] = c + u < n ? ex2_approx((lrow[cu] - m) * kLog2e) : 0.f;
+                for (int i = 0; i < V; ++i) acc[i] = fmaf(w, v[u][i], acc[i]);
             }
+            const float inv = 1.0f / s;
 #pragma unroll
-            for (int u = 0; u < NB; ++u)
-#pragma unroll
-                for (int i = 0; i < V; ++i) acc[i] = fmaf(w[u], v[u][i], acc[i]);
+            for (int i = 0; i < V; ++i) acc[i] *= inv;
+            lse = m + lg2_approx(s) * 0.69314718055994531f;
         }
-        const float inv = 1.0f / s;
+    } else if (n > NB) {
+        float m = kNegInf;
+        for (int c = lane; c < n; c += 32) m = fmaxf(m, lrow[c]);
 #pragma unroll
-        for (int i = 0; i < V; ++i) acc[i] *= inv;
-        lse = m + lg2_approx(s) * 0.69314718055994531f;
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (m != kNegInf) {
+            float s = 0.f;
+            for (int c = 0; c < n; c += NB) {
+                float v[NB][V];
+                float w[NB];
+#pragma unroll
+                for (int u = 0; u < NB; ++u) {
+                    const int cu = min(c + u, n - 1);
+#pragma unroll
+                    for (int i = 0; i < V; ++i) v[u][i] = orow[(size_t)cu * D + i * 32];
+                    w[u] = c + u < n ? ex2_approx((lrow[cu] - m) * kLog2e) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < NB; ++u) {
+                    s += w[u];
+#pragma unroll
+                    for (int i = 0; i < V; ++i) acc[i] = fmaf(w[u], v[u][i], acc[i]);
+                }
+            }
+            const float inv = 1.0f / s;
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] *= inv;
+            lse = m + lg2_approx(s) * 0.69314718055994531f;
+        }
     }
     uint16_t* out = reinterpret_cast<uint16_t*>(p.o) + (size_t)bh * D + lane;
 #pragma unroll
