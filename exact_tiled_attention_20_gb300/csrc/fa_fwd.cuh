@@ -732,23 +732,58 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     (n0 + C::BN > c.sk) ||
                     (p.has_hi && (n0 + C::BN - 1 > tile_row0 + off + p.hi_off)) ||
                     (p.has_lo && (n0 < tile_row0 + C::BM - 1 + off - p.win_left));
+                // Two ways to mask (both exact).  The general fixed-length kernels compare
+                // and select per score on the integer pipe.  The others (sliding windows,
+                // packed variable-length batches, S ahead of P.V) add 2^126 times a mask
+                // bit t (1: masked) that one saturating add computes on the FMA pipe: s -
+                // 2^126 is about -2^126 for any finite s, and its exponential 0.  The column
+                // and the bounds (clamped to [-1, BN]) are small integers, so t is exactly 0
+                // or 1.  A row with every score of the block masked then has no maximum here.
+                constexpr bool kFmaMask = kSkip || kVarlen || C::kSAhead;
                 if (need_mask) {
                     int kmax = c.sk - 1 - n0;
                     if (p.has_hi) kmax = min(kmax, row + off + p.hi_off - n0);
+                    constexpr float kS = 18446744073709551616.0f;    // 2^64
+                    constexpr float kOut = -8.5070591730234616e37f;  // -2^126
                     // (the window instantiation always has a lower bound, and keeps the one loop)
                     if (kSkip || p.has_lo) {
                         const int kmin = p.has_lo ? row + off - p.win_left - n0 : -1;
+                        if constexpr (kFmaMask) {
+                            // masked iff |col - mid| > half the width of [kmin, kmax]
+                            const float lo = (float)min(max(kmin, -1), C::BN), hi = (float)min(max(kmax, -1), C::BN);
+                            const float mid = (lo + hi) * (0.5f * kS);
+                            const float half = ((hi - lo) * 0.5f + 0.5f) * kS;
 #pragma unroll
-                        for (int ch = 0; ch < kSC; ++ch)
+                            for (int ch = 0; ch < kSC; ++ch)
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                u[ch][i] = ((ch * 32 + i > kmax) | (ch * 32 + i < kmin)) ? 0xff800000u : u[ch][i];
-                    } else {  // no lower bound: one comparison per score
+                                for (int i = 0; i < 32; ++i) {
+                                    const float t = __saturatef(fabsf((float)(ch * 32 + i) * kS - mid) - half);
+                                    u[ch][i] = __float_as_uint(fmaf(t, kOut, __uint_as_float(u[ch][i])));
+                                }
+                        } else {
 #pragma unroll
-                        for (int ch = 0; ch < kSC; ++ch)
+                            for (int ch = 0; ch < kSC; ++ch)
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                u[ch][i] = (ch * 32 + i > kmax) ? 0xff800000u : u[ch][i];
+                                for (int i = 0; i < 32; ++i)
+                                    u[ch][i] = ((ch * 32 + i > kmax) | (ch * 32 + i < kmin)) ? 0xff800000u : u[ch][i];
+                        }
+                    } else {  // no lower bound: masked iff col > kmax
+                        if constexpr (kFmaMask) {
+                            const float edge = ((float)min(max(kmax, -1), C::BN) + 0.5f) * kS;
+#pragma unroll
+                            for (int ch = 0; ch < kSC; ++ch)
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) {
+                                    const float t = __saturatef((float)(ch * 32 + i) * kS - edge);
+                                    u[ch][i] = __float_as_uint(fmaf(t, kOut, __uint_as_float(u[ch][i])));
+                                }
+                        } else {
+#pragma unroll
+                            for (int ch = 0; ch < kSC; ++ch)
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    u[ch][i] = (ch * 32 + i > kmax) ? 0xff800000u : u[ch][i];
+                        }
                     }
                 }
                 // Row max over the BN scores: four independent chains of 3-input maxima.
@@ -762,7 +797,9 @@ __global__ void __launch_bounds__(C::kThreads, 1)
                     for (int c4 = 0; c4 < 4; ++c4) mx[c4] = max3f(mx[c4], sv(k + c4), sv(k + c4 + 4));
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) mx[c4] = fmaxf(mx[c4], sv(C::BN - 4 + c4));
-                const float m_blk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
+                const float raw_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                const float m_blk =
+                    (kFmaMask && raw_max < -4.2535295865117308e37f) ? kNegInf : raw_max * p.scale_log2;
                 const bool bump = m_blk > m_run + kRescaleLog2;
                 const float m_new = bump ? m_blk : m_run;
                 const float alpha = bump ? ex2_approx(m_run - m_new) : 1.0f;
