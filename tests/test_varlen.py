@@ -53,6 +53,7 @@ CASES = [
     ([200, 260], [0, 260], 2, 2, 64, False, (-1, -1)),                # a sequence with no keys
     ([511, 64], [511, 64], 2, 1, 96, True, (50, 0)),
     ([384, 129], [384, 129], 2, 2, 256, False, (20, 30)),
+    ([300, 0, 90], [40, 7, 300], 2, 1, 64, True, (-1, -1)),          # rows with no visible key
 ]
 
 

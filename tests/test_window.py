@@ -61,6 +61,9 @@ CASES = [
     (2, 1030, 1030, 2, 2, 128, 127, 0, True),   # short window: most blocks dead for one sub-tile
     (1, 1100, 1100, 2, 1, 96, 200, 0, False),   # D = 96, several tiles
     (1, 300, 300, 2, 1, 128, 50, 0, False),     # last tile's second sub-tile lies past Sq
+    # D = 64 (general kernel, FMA-pipe mask with two bounds):
+    (1, 500, 120, 2, 1, 64, 30, 5, False),      # Sq > Sk: leading rows see no key
+    (1, 600, 600, 2, 2, 64, 130, 0, True),
 ]
 
 
